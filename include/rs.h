@@ -1,0 +1,230 @@
+/*
+ * rs.h - C ABI of librs, a single-GPU library for the ReplaySSM decode path
+ * (Mamba-2 and Gated DeltaNet layers) with hand-written sm_103a kernels.
+ *
+ * The method ("ReplaySSM: Cache SSM Inputs, Not State", section "How it
+ * works"; the paper abstract on the same subject) keeps each sequence's
+ * recurrent state S (P x N per head) as
+ *
+ *     a checkpoint S_c  +  a circular buffer of the SSM inputs since S_c,
+ *
+ * so that after h buffered records S = gamma * S_c + sum_j w_j v_j k_j^T,
+ * with w_j the product of the decays after record j and gamma the product of
+ * all of them.  A decode step appends its record and computes its output
+ * straight from that form, without writing the state back; the checkpoint is
+ * written only when the buffer reaches the window size L ("flush").
+ * Speculative verification appends T draft records and computes all T
+ * outputs from one checkpoint read; accepting a prefix or rolling back only
+ * moves pointers.
+ *
+ * ---------------------------------------------------------------- conventions
+ * Ownership: the caller allocates every buffer (device memory unless stated)
+ *   and passes raw pointers; rs_state_bytes() gives the sizes.  The library
+ *   allocates nothing and keeps no global state.  All pointers to device
+ *   arrays must be 16-byte aligned.
+ * Streams: every call that touches the GPU takes a stream (a cudaStream_t,
+ *   passed as void*; NULL = legacy default stream) and only enqueues work on
+ *   it, except rs_get_status, which synchronises that stream.
+ * Errors: every call returns rs_status and never aborts.  Argument problems
+ *   found on the host return RS_ERR_INVALID_ARG / RS_ERR_UNSUPPORTED before
+ *   anything is enqueued.  A failed launch returns RS_ERR_CUDA.  Problems only
+ *   visible on the device (a pointer state that breaks a rule below) set bits
+ *   of the device status word, which rs_get_status reads; kernels never trap.
+ * Types: "bf16" arrays are passed as raw 16-bit patterns (uint16_t); fp32 is
+ *   float.  Outputs y are fp32.
+ *
+ * Layouts (row-major, innermost last):
+ *   checkpoint (both precisions)  [B][H][N][P]   key index n, then value index p
+ *   Mamba-2 step inputs  x [B][T][H][P] bf16, dt [B][T][H] f32,
+ *                        Bm, Cm [B][T][G][N] bf16, A [H] f32, D [H] f32
+ *   GDN step inputs      q, k [B][T][G][N] bf16 (k-heads), v [B][T][H][P] bf16,
+ *                        alpha, beta [B][T][H] f32
+ *   outputs              y [B][T][H][P] f32
+ *   (T = 1 for the decode calls; the T axis may then be left out.)
+ *   Mamba-2 head h uses B/C group h / (H/G); GDN v-head h uses k-head h / (H/G).
+ */
+#ifndef RS_H
+#define RS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RS_OK = 0,
+    RS_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or count   */
+    RS_ERR_UNSUPPORTED = 2,  /* shape or mode without a kernel instantiation */
+    RS_ERR_CAPACITY = 3,     /* capacity too small for L + T_max             */
+    RS_ERR_CUDA = 4,         /* a CUDA call failed (launch or copy)          */
+    RS_ERR_DEVICE = 5        /* the device status word has bits set          */
+} rs_status;
+
+/* Bits of the device status word. */
+#define RS_DEV_CAPACITY 0x1u       /* records would overflow the circular buffer; sequence skipped */
+#define RS_DEV_ACCEPT 0x2u         /* accepted length outside 0..nd; clamped                     */
+#define RS_DEV_DRAFTS_PENDING 0x4u /* decode/verify/append with uncommitted drafts; drafts dropped */
+
+typedef enum { RS_MAMBA2 = 0, RS_GDN = 1 } rs_kind;
+
+typedef enum {
+    RS_PREC_FP32 = 0,        /* fp32 checkpoint only                                          */
+    RS_PREC_TWO = 1,         /* fp32 high-precision copy + bf16 low-precision copy: non-flush
+                                steps read bf16, flushes read fp32 and write both             */
+    RS_PREC_SHARED_BF16 = 2  /* one bf16 checkpoint serves reads and updates                  */
+} rs_precision;
+
+/* Shape of one layer.  Supported (P, N): Mamba-2 (64,128), (64,64);
+ * GDN (128,128), (64,64).  L >= 1, T_max in 0..8, L + T_max <= capacity <= 32. */
+typedef struct {
+    int32_t kind;      /* rs_kind                                              */
+    int32_t B;         /* sequences                                            */
+    int32_t H;         /* Mamba-2 heads / GDN value heads                      */
+    int32_t G;         /* Mamba-2 B/C groups / GDN key heads; H % G == 0       */
+    int32_t P;         /* Mamba-2 headdim / GDN d_v                            */
+    int32_t N;         /* Mamba-2 dstate / GDN d_k                             */
+    int32_t L;         /* window: a standard step flushes when it makes h >= L */
+    int32_t T_max;     /* largest draft count of rs_verify (0: standard only)  */
+    int32_t capacity;  /* circular buffer slots per sequence                   */
+    int32_t precision; /* rs_precision                                         */
+} rs_layer_desc;
+
+/* Per-layer state; every member is a caller-allocated device array. */
+typedef struct {
+    float *ckpt_hp;    /* fp32 checkpoint [B][H][N][P]; NULL for RS_PREC_SHARED_BF16 */
+    uint16_t *ckpt_lp; /* bf16 checkpoint [B][H][N][P]; NULL for RS_PREC_FP32        */
+    void *buf_v;       /* records' values: Mamba-2 x bf16 [B][cap][H][P];
+                          GDN correction term u fp32 [B][cap][H][P]                   */
+    uint16_t *buf_k;   /* records' keys (Mamba-2 B / GDN k) bf16 [B][cap][G][N]       */
+    float *buf_a;      /* records' decays alpha, fp32 [B][cap][H] (Mamba-2: exp(dt A))  */
+    float *buf_s;      /* Mamba-2 records' dt, fp32 [B][cap][H] (v = dt x); NULL for GDN */
+    int32_t *base;     /* [B] slot of the first record after the checkpoint          */
+    int32_t *h;        /* [B] committed records after the checkpoint                 */
+    int32_t *nd;       /* [B] appended, not yet accepted draft records               */
+    uint32_t *arrive;  /* [B] per-sequence arrival counters (kernel scratch)         */
+    uint32_t *status;  /* [1] device status word (RS_DEV_* bits)                     */
+} rs_state;
+
+/* Byte sizes of the rs_state arrays for a descriptor (0 for an unused array). */
+typedef struct {
+    size_t ckpt_hp, ckpt_lp, buf_v, buf_k, buf_a, buf_s, base, h, nd, arrive, status;
+} rs_state_bytes;
+
+/* Inputs of several records per sequence, [B][n][...] as in the layouts above.
+ * Members of the other family must be NULL. */
+typedef struct {
+    const uint16_t *x;  const float *dt; const float *A;
+    const uint16_t *Bm; const uint16_t *Cm; const float *D; /* D may be NULL (= 0) */
+    const uint16_t *q;  const uint16_t *k;  const uint16_t *v;
+    const float *alpha; const float *beta;
+} rs_inputs;
+
+/* ------------------------------------------------------------------- host-only */
+const char *rs_status_string(rs_status s);
+const char *rs_version(void);
+
+/* Validates the descriptor and fills the array sizes.  Host only. */
+rs_status rs_state_bytes_for(const rs_layer_desc *desc, rs_state_bytes *out);
+
+/* ---------------------------------------------------------------- state setup */
+/* Writes the checkpoint from init (fp32 [B][H][N][P], device; NULL = zeros):
+ * the fp32 copy and/or its bf16 rounding (nearest-even) per the precision
+ * mode.  Clears base, h, nd, the arrival counters and the status word.
+ * This is the two-precision checkpoint writer on its own ("Two precisions"
+ * bullet, section "How it works"). */
+rs_status rs_init(const rs_layer_desc *desc, const rs_state *st, const float *init, void *stream);
+
+/* Reads the device status word into *bits (host), after synchronising the
+ * stream; clears it if clear != 0.  Returns RS_ERR_DEVICE if any bit was set. */
+rs_status rs_get_status(const rs_state *st, uint32_t *bits, int clear, void *stream);
+
+/* ------------------------------------------------------------ standard decode */
+/* One Mamba-2 decode step for all B sequences ("How it works", standard
+ * decoding bullet).  Per sequence: append the record (x_t, dt_t, B_t) and
+ * write y_t = gamma S_c C_t + sum_j w_j dt_j x_j (B_j . C_t) + D x_t without
+ * writing the state.  When the record makes h >= L the same launch folds all
+ * h records into the checkpoint, S_c <- gamma S_c + V diag(w) K^T ("flush
+ * route"), and resets h to 0.  alpha_t = exp(dt_t A_h).
+ * Drafts pending are dropped (RS_DEV_DRAFTS_PENDING). */
+rs_status rs_decode_mamba2(const rs_layer_desc *desc, const rs_state *st, const uint16_t *x,
+                           const float *dt, const float *A, const uint16_t *Bm,
+                           const uint16_t *Cm, const float *D, float *y, void *stream);
+
+/* One Gated DeltaNet decode step ("How it works", Gated DeltaNet bullet):
+ * u_t = beta_t (v_t - alpha_t S_{t-1} k_t) where S_{t-1} k_t is itself
+ * replayed from the checkpoint and the buffered u_j; the record stores u_t in
+ * place of v_t; y_t = S_t q_t.  One checkpoint read serves both S k and S q.
+ * Flush rule as for rs_decode_mamba2. */
+rs_status rs_decode_gdn(const rs_layer_desc *desc, const rs_state *st, const uint16_t *q,
+                        const uint16_t *k, const uint16_t *v, const float *alpha,
+                        const float *beta, float *y, void *stream);
+
+/* ------------------------------------------------------------------ speculative */
+/* Speculative verification of T drafts (1 <= T <= T_max), either family
+ * ("How it works", speculative bullet and flowchart).  Appends the T draft
+ * records and writes all T outputs y [B][T][H][P] from one checkpoint read
+ * and the buffer.  Per sequence, if h + T > L the committed records (never
+ * the drafts) are folded into the checkpoint in the same launch (reading the
+ * fp32 copy and writing both copies in two-precision mode); otherwise the
+ * low-precision copy is read in two-precision mode.  Sets nd = T. */
+rs_status rs_verify(const rs_layer_desc *desc, const rs_state *st, int T, const rs_inputs *in,
+                    float *y, void *stream);
+
+/* Accepts a prefix of the drafts: h += accepted[b], nd = 0 (a pointer move).
+ * accepted: device int32 [B], each in 0..nd (else clamped, RS_DEV_ACCEPT). */
+rs_status rs_commit(const rs_layer_desc *desc, const rs_state *st, const int32_t *accepted,
+                    void *stream);
+
+/* Discards the drafts: nd = 0.  Their records are overwritten later. */
+rs_status rs_rollback(const rs_layer_desc *desc, const rs_state *st, void *stream);
+
+/* ---------------------------------------------------------------- maintenance */
+/* Appends n committed Mamba-2 records per sequence without computing outputs
+ * or flushing (x, dt, Bm of in, each [B][n][...]).  Needs nd == 0 and
+ * h + n <= capacity per sequence (else that sequence is skipped and a status
+ * bit set).  GDN records depend on the state, so GDN returns RS_ERR_UNSUPPORTED. */
+rs_status rs_append(const rs_layer_desc *desc, const rs_state *st, int n, const rs_inputs *in,
+                    void *stream);
+
+/* Folds every committed record into the checkpoint now (h -> 0), writing
+ * both copies in two-precision mode.  Drafts stay appended. */
+rs_status rs_flush(const rs_layer_desc *desc, const rs_state *st, void *stream);
+
+/* Writes the committed state S = gamma S_c + sum_{j<h} w_j v_j k_j^T to out
+ * (fp32 [B][H][N][P], device) without changing anything; an export of the
+ * current state, e.g. for prefix caching. */
+rs_status rs_materialize(const rs_layer_desc *desc, const rs_state *st, float *out, void *stream);
+
+/* ---------------------------------------------------------- eager baselines */
+/* Conventional decode that loads and stores the state every step (the
+ * baseline of the thread's post [2/N] and of the abstract): S <- alpha S +
+ * v k^T, y = S q (+ D x).  S: fp32 [B][H][N][P], updated in place.  Only
+ * kind, B, H, G, P, N of desc are used. */
+rs_status rs_eager_step_mamba2(const rs_layer_desc *desc, float *S, const uint16_t *x,
+                               const float *dt, const float *A, const uint16_t *Bm,
+                               const uint16_t *Cm, const float *D, float *y, void *stream);
+rs_status rs_eager_step_gdn(const rs_layer_desc *desc, float *S, const uint16_t *q,
+                            const uint16_t *k, const uint16_t *v, const float *alpha,
+                            const float *beta, float *y, void *stream);
+
+/* Per-draft snapshot baseline for speculative decoding (the thread's post
+ * [3/N]: one state kept per draft token).  pool: fp32 [B][T_max+1][H][N][P];
+ * cur: device int32 [B], the pool slot holding each sequence's committed state.
+ * Reads slot cur[b], runs the eager recurrence over the T drafts, writes each
+ * intermediate state to slot (cur[b] + 1 + i) % (T_max + 1) and the outputs to
+ * y [B][T][H][P]. */
+rs_status rs_eager_verify_snapshots(const rs_layer_desc *desc, float *pool, const int32_t *cur,
+                                    int T, const rs_inputs *in, float *y, void *stream);
+
+/* Selects the snapshot of the accepted prefix: cur[b] = (cur[b] +
+ * accepted[b]) % (T_max + 1).  status (device [1], may be NULL) gets
+ * RS_DEV_ACCEPT for an accepted length outside 0..T_max. */
+rs_status rs_eager_select(const rs_layer_desc *desc, int32_t *cur, const int32_t *accepted,
+                          uint32_t *status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RS_H */

@@ -1,0 +1,148 @@
+// Device-side building blocks shared by the librs kernels: bf16 <-> fp32
+// conversion, streaming 128-bit memory access, the per-thread tile geometry
+// of a (N x P) checkpoint slab, and a CTA reduction over threads that own the
+// same value columns.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "rs.h"
+
+namespace rs {
+
+constexpr int kMaxCap = 32;  // circular buffer slots per sequence (one warp lane per record)
+constexpr int kMaxT = 8;     // drafts per verify launch
+
+enum Mode { MODE_DECODE = 0, MODE_VERIFY = 1, MODE_FLUSH = 2, MODE_MATERIALIZE = 3 };
+
+// ---------------------------------------------------------------- conversions
+__device__ __forceinline__ float bf2f(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+__device__ __forceinline__ uint32_t f2bf(float f) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) { return f2bf(lo) | (f2bf(hi) << 16); }
+
+// ---------------------------------------------------------------- memory
+// The checkpoint is touched once per launch: stream it past the caches
+// (evict-first) so the small, re-read buffer records stay resident in L2.
+__device__ __forceinline__ uint4 ld_stream(const void *p) { return __ldcs(reinterpret_cast<const uint4 *>(p)); }
+__device__ __forceinline__ void st_stream(void *p, uint4 v) { __stcs(reinterpret_cast<uint4 *>(p), v); }
+__device__ __forceinline__ void st_stream2(void *p, uint2 v) { __stcs(reinterpret_cast<uint2 *>(p), v); }
+__device__ __forceinline__ uint4 ld_u4(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
+
+// ---------------------------------------------------------------- tile geometry
+// A (N x P) checkpoint slab is row-major with P contiguous.  A thread owns VEC
+// consecutive value columns (one 16-byte vector) of R consecutive key rows:
+// TPR threads cover one row, the CTA's NT threads cover RG = NT/TPR row
+// groups.  Every row is a contiguous P*sizeof(TE)-byte segment, so each warp
+// load instruction reads 32/TPR whole rows.
+template <typename TE> struct Vec;
+template <> struct Vec<float> { static constexpr int n = 4; };
+template <> struct Vec<uint16_t> { static constexpr int n = 8; };
+
+template <int P, int N, int NT, typename TE> struct Geo {
+    static constexpr int VEC = Vec<TE>::n;
+    static constexpr int TPR = P / VEC;
+    static constexpr int RG = NT / TPR;
+    static constexpr int R = N / RG;
+    static_assert(P % VEC == 0 && TPR <= 32 && 32 % TPR == 0, "row must map onto a warp fraction");
+    static_assert(NT % TPR == 0 && N % RG == 0 && R >= 1, "rows must split evenly over row groups");
+};
+
+template <typename TE, int VEC>
+__device__ __forceinline__ void unpack(const uint4 &u, float (&f)[VEC]);
+template <> __device__ __forceinline__ void unpack<float, 4>(const uint4 &u, float (&f)[4]) {
+    f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+}
+template <> __device__ __forceinline__ void unpack<uint16_t, 8>(const uint4 &u, float (&f)[8]) {
+    f[0] = bf2f(u.x & 0xffffu); f[1] = __uint_as_float(u.x & 0xffff0000u);
+    f[2] = bf2f(u.y & 0xffffu); f[3] = __uint_as_float(u.y & 0xffff0000u);
+    f[4] = bf2f(u.z & 0xffffu); f[5] = __uint_as_float(u.z & 0xffff0000u);
+    f[6] = bf2f(u.w & 0xffffu); f[7] = __uint_as_float(u.w & 0xffff0000u);
+}
+
+// Store VEC fp32 values to an fp32 array (16 or 32 bytes).
+template <int VEC>
+__device__ __forceinline__ void store_f32(float *dst, const float (&f)[VEC]) {
+#pragma unroll
+    for (int c = 0; c < VEC / 4; ++c)
+        st_stream(dst + 4 * c, make_uint4(__float_as_uint(f[4 * c]), __float_as_uint(f[4 * c + 1]),
+                                          __float_as_uint(f[4 * c + 2]), __float_as_uint(f[4 * c + 3])));
+}
+// Store VEC values rounded to bf16 (8 or 16 bytes).
+template <int VEC>
+__device__ __forceinline__ void store_bf16(uint16_t *dst, const float (&f)[VEC]) {
+    if constexpr (VEC == 4) {
+        st_stream2(dst, make_uint2(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3])));
+    } else {
+        st_stream(dst, make_uint4(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]), pack_bf2(f[4], f[5]),
+                                  pack_bf2(f[6], f[7])));
+    }
+}
+
+// Copy `count` bf16 values (count % 8 == 0, 16-byte aligned) into fp32 shared memory.
+__device__ __forceinline__ void bf16_row_to_smem(float *dst, const uint16_t *src, int count, int lane0,
+                                                 int stride) {
+    for (int c = lane0; c < count / 8; c += stride) {
+        uint4 u = ld_u4(src + 8 * c);
+        float f[8];
+        unpack<uint16_t, 8>(u, f);
+        float4 *d = reinterpret_cast<float4 *>(dst + 8 * c);
+        d[0] = make_float4(f[0], f[1], f[2], f[3]);
+        d[1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
+}
+
+// ---------------------------------------------------------------- CTA reduction
+// Each thread holds acc[NV][VEC] partial sums for value columns pv*VEC..+VEC of
+// NV vectors.  Sums over all threads with the same pv and leaves the totals
+// in red[v*P + p] (v < nv), using red[NW][NV*P] as scratch.  Call from all
+// threads; contains two __syncthreads.
+template <int NT, int TPR, int VEC, int P, int NV>
+__device__ __forceinline__ void cta_reduce(float (&acc)[NV][VEC], int nv, float *red) {
+    constexpr int NW = NT / 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (int off = TPR; off < 32; off <<= 1)
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) acc[v][e] += __shfl_xor_sync(0xffffffffu, acc[v][e], off);
+    if (lane < TPR) {
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            if (v < nv) {
+                float *d = red + ((size_t)warp * nv + v) * P + lane * VEC;
+#pragma unroll
+                for (int c = 0; c < VEC / 4; ++c)
+                    reinterpret_cast<float4 *>(d)[c] =
+                        make_float4(acc[v][4 * c], acc[v][4 * c + 1], acc[v][4 * c + 2], acc[v][4 * c + 3]);
+            }
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < nv * P; i += NT) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) s += red[(size_t)w * nv * P + i];
+        red[i] = s;
+    }
+    __syncthreads();
+}
+
+// Per-sequence arrival: every CTA of sequence b calls this exactly once per
+// launch (thread 0, after the CTA has finished reading the pointers).
+// Returns true in the last CTA to arrive, which may then update the
+// sequence's pointers; the counter wraps back to 0 for the next launch.
+__device__ __forceinline__ bool arrive_last(uint32_t *counter, unsigned ctas_per_seq) {
+    __threadfence();
+    const unsigned prev = atomicInc(counter, ctas_per_seq - 1);
+    const bool last = prev == ctas_per_seq - 1;
+    if (last) __threadfence();
+    return last;
+}
+
+}  // namespace rs

@@ -1,0 +1,128 @@
+"""GPU parity of speculative verification, commit and rollback against the
+fp64 oracle (eager recurrence over the drafts, commit of the accepted prefix).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from harness import TOL_HP, TOL_LP, SpecRun, rel_err, state_gpu_to_np
+from rs_decode_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_spec(w, rounds, seed=0, precision=None, sample=None, accept=None):
+    run = SpecRun(w, seed=seed, precision=precision, sample=sample)
+    prec = precision or w.precision
+    errs = []
+    nfold = 0
+    for r in range(rounds):
+        a = None if accept is None else accept(r, w.B)
+        y, y_ref, folded, S_before, acc = run.round(a)
+        e = rel_err(y.reshape(len(run.idx), -1), y_ref.reshape(len(run.idx), -1))
+        tol = np.where(folded | (prec == "fp32"), TOL_HP, TOL_LP) if prec != "shared_bf16" else TOL_LP
+        assert (e <= tol).all(), f"round {r}: verify rel err {e.max():.3e}"
+        errs.append(e)
+        if folded.any():
+            nfold += int(folded.sum())
+            ck = run.layer.checkpoint_hp()
+            ck = ck if ck is not None else run.layer.checkpoint_lp_f32()
+            got = state_gpu_to_np(ck[torch.from_numpy(run.idx).cuda()])
+            ce = rel_err(got[folded], S_before[folded])
+            assert ce.max() <= (TOL_HP if prec != "shared_bf16" else TOL_LP), f"round {r}: fold {ce.max():.3e}"
+        if prec != "shared_bf16":
+            m = rel_err(state_gpu_to_np(run.layer.materialize()[torch.from_numpy(run.idx).cuda()]), run.model.S)
+            assert m.max() <= TOL_HP, f"round {r}: committed state rel err {m.max():.3e}"
+    ptr = run.layer.pointers()
+    assert (ptr["h"][run.idx] == [run.ptrs[b].h for b in run.idx]).all()
+    assert (ptr["base"][run.idx] == [run.ptrs[b].base for b in run.idx]).all()
+    assert run.layer.status() == 0
+    return np.concatenate(errs), nfold
+
+
+def test_mamba2_spec_small_batch():
+    w = synth.WORKLOADS["mamba2_spec"].with_(B=8)
+    _, nfold = _run_spec(w, 14, seed=1)
+    assert nfold > 0
+
+
+def test_gdn_spec_two_precision_small_batch():
+    w = synth.WORKLOADS["gdn_spec"].with_(B=8)
+    _, nfold = _run_spec(w, 14, seed=2)
+    assert nfold > 0
+
+
+@pytest.mark.parametrize("kind", ["mamba2", "gdn"])
+def test_two_precision_beats_shared_bf16(kind):
+    """Separate precisions keep bf16 rounding out of the recurrence, so their
+    output error does not exceed that of a shared bf16 checkpoint."""
+    base = synth.WORKLOADS["gdn_spec" if kind == "gdn" else "mamba2_spec"].with_(B=6)
+    e_two, _ = _run_spec(base, 24, seed=3, precision="two")
+    e_shared, _ = _run_spec(base, 24, seed=3, precision="shared_bf16")
+    assert np.mean(e_two) <= np.mean(e_shared)
+
+
+@pytest.mark.parametrize("kind", ["mamba2", "gdn"])
+def test_spec_full_batch_sampled(kind):
+    w = synth.WORKLOADS["gdn_spec" if kind == "gdn" else "mamba2_spec"]
+    _run_spec(w, 6, seed=0, sample=[0, 3, 255, w.B - 1])
+
+
+@pytest.mark.parametrize("T", [1, 2, 8])
+def test_draft_counts(T):
+    w = synth.WORKLOADS["tiny"].with_(B=3, T=T, capacity=16 + T, accept="uniform")
+    _run_spec(w, 12, seed=4 + T)
+
+
+def test_reject_everything_keeps_checkpoint():
+    """a = 0 every round: nothing is committed, the checkpoint never changes."""
+    w = synth.WORKLOADS["mamba2_spec"].with_(B=3)
+    run = SpecRun(w, seed=5)
+    ck0 = run.layer.checkpoint_hp().clone()
+    for r in range(6):
+        y, y_ref, folded, _, _ = run.round(np.zeros(w.B, np.int32))
+        assert rel_err(y.reshape(w.B, -1), y_ref.reshape(w.B, -1)).max() <= TOL_HP
+        assert not folded.any()
+    assert torch.equal(run.layer.checkpoint_hp(), ck0)
+    assert (run.layer.pointers()["h"] == 0).all()
+
+
+def test_accept_all_equals_standard_decode():
+    """T = 1 with every draft accepted reproduces standard decode outputs."""
+    w = synth.WORKLOADS["tiny"].with_(B=2, T=1, capacity=17, accept="uniform")
+    run = SpecRun(w, seed=6)
+    for r in range(40):
+        y, y_ref, _, _, _ = run.round(np.ones(w.B, np.int32))
+        assert rel_err(y.reshape(w.B, -1), y_ref.reshape(w.B, -1)).max() <= TOL_HP
+
+
+def test_rollback_then_verify_again():
+    """rs_rollback discards drafts: re-verifying from the same committed state
+    gives the same outputs."""
+    from rs_decode_gb300.layer import to_device
+    w = synth.WORKLOADS["mamba2_spec"].with_(B=2)
+    run = SpecRun(w, seed=7)
+    run.round()
+    d = to_device(synth.round_inputs(w, 99, 7, run.params))
+    y1 = run.layer.verify(w.T, d, run.gp).clone()
+    run.layer.rollback()
+    assert (run.layer.pointers()["nd"] == 0).all()
+    y2 = run.layer.verify(w.T, d, run.gp)
+    run.layer.rollback()
+    assert torch.equal(y1, y2)
+    assert run.layer.status() == 0
+
+
+def test_bad_accept_sets_status_bit():
+    from rs_decode_gb300 import binding as rb
+    w = synth.WORKLOADS["mamba2_spec"].with_(B=2)
+    run = SpecRun(w, seed=8)
+    d = synth.round_inputs(w, 0, 8, run.params)
+    from rs_decode_gb300.layer import to_device
+    run.layer.verify(w.T, to_device(d), run.gp)
+    run.layer.commit(torch.tensor([w.T + 3, -1], dtype=torch.int32, device="cuda"))
+    assert run.layer.status() & rb.DEV_ACCEPT
+    ptr = run.layer.pointers()
+    assert list(ptr["h"]) == [w.T, 0] and (ptr["nd"] == 0).all()
