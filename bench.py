@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-eager", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="sequences per GPU (default: the workload's 256; smaller only for profiling)")
     return ap.parse_args()
 
 
@@ -146,6 +149,26 @@ class ClockSampler:
                 "power_w_max": max(float(r[4]) for r in sel if r[4].strip().replace(".", "").isdigit())}
 
 
+# ----------------------------------------------------------------------------- ranks
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value over all ranks (the job's time is its slowest rank's).
+    Without an initialised process group this is x itself."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    if device is None or dist.get_backend() == "gloo":
+        device = torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(rank: int) -> int:
+    """Each rank decodes its own, independently seeded sequences (weak scaling)."""
+    return rank
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 def time_oracle(w, seconds: float, batch: int = 16):
     """fp64 oracle on the host cores: batch sequences of the workload, as many
@@ -180,11 +203,13 @@ def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     w = synth.WORKLOADS[WORKLOAD]
+    if args.batch:
+        w = w.with_(B=args.batch)
     K, W = args.steps, args.warmup
     params = synth.layer_params(w)
     gp = {"A": torch.from_numpy(params["A"]).to(dev), "D": torch.from_numpy(params["D"]).to(dev)}
     npool = min(INPUT_POOL, K + W)
-    host_steps = [synth.step_inputs(w, s, seed=rank, params=params) for s in range(npool)]
+    host_steps = [synth.step_inputs(w, s, seed=rank_seed(rank), params=params) for s in range(npool)]
     dev_steps = [to_device(d, dev) for d in host_steps]
 
     layer = Layer("mamba2", w.B, w.H, w.G, w.P, w.N, w.L)
@@ -234,23 +259,25 @@ def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
         h = 0 if flush else h + 1
 
     # ---- eager baseline on the same workload
-    S_eager = S0.clone()
-    desc = layer.desc
-    Ke = min(K, 512)
-    def eager(s):
-        d = dev_steps[s % npool]
-        rb.rs_eager_step_mamba2(desc, S_eager, d["x"], d["dt"], gp["A"], d["Bm"], d["Cm"], gp["D"], y)
-    for s in range(W):
-        eager(s)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for s in range(Ke):
-        eager(W + s)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms_eager = e0.elapsed_time(e1) / Ke
-    del S_eager
+    ms_eager = None
+    if not args.no_eager:
+        S_eager = S0.clone()
+        desc = layer.desc
+        Ke = min(K, 512)
+        def eager(s):
+            d = dev_steps[s % npool]
+            rb.rs_eager_step_mamba2(desc, S_eager, d["x"], d["dt"], gp["A"], d["Bm"], d["Cm"], gp["D"], y)
+        for s in range(W):
+            eager(s)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(Ke):
+            eager(W + s)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_eager = e0.elapsed_time(e1) / Ke
+        del S_eager
 
     # ---- end to end through host buffers (pinned), copies inside the timed region
     e2e = None
@@ -282,10 +309,7 @@ def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
                "d2h_bytes_per_step": bo, "ms_per_step": ms_x}
 
     # ---- max over ranks
-    t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dev)
     if rank != 0:
         return None
 
@@ -321,9 +345,10 @@ def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
                      "algorithmic_bytes_per_launch": total_bytes / K,
                      "kernel": "replay_kernel<mamba2,64,128,HPC=2,TMAX=1,256>"},
         "hbm_gbs": achieved,
-        "eager": {"ms_per_step": ms_eager, "value": w.B / (ms_eager * 1e-3), "unit": "tokens/s",
-                  "achieved_gbs": eager_bytes / (ms_eager * 1e-3) / 1e9,
-                  "bytes_per_step": eager_bytes, "speedup_of_replay": ms_eager / (ms_total / K)},
+        "eager": None if ms_eager is None else {
+            "ms_per_step": ms_eager, "value": w.B / (ms_eager * 1e-3), "unit": "tokens/s",
+            "achieved_gbs": eager_bytes / (ms_eager * 1e-3) / 1e9,
+            "bytes_per_step": eager_bytes, "speedup_of_replay": ms_eager / (ms_total / K)},
         "gpu_launches": K,
         "clocks": clk,
         "e2e": e2e,

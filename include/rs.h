@@ -66,6 +66,7 @@ typedef enum {
 #define RS_DEV_CAPACITY 0x1u       /* records would overflow the circular buffer; sequence skipped */
 #define RS_DEV_ACCEPT 0x2u         /* accepted length outside 0..nd; clamped                     */
 #define RS_DEV_DRAFTS_PENDING 0x4u /* decode/verify/append with uncommitted drafts; drafts dropped */
+#define RS_DEV_TIMEOUT 0x8u        /* an in-kernel wait gave up after its time limit; results invalid */
 
 typedef enum { RS_MAMBA2 = 0, RS_GDN = 1 } rs_kind;
 

@@ -32,6 +32,99 @@ __device__ __forceinline__ void st_stream(void *p, uint4 v) { __stcs(reinterpret
 __device__ __forceinline__ void st_stream2(void *p, uint2 v) { __stcs(reinterpret_cast<uint2 *>(p), v); }
 __device__ __forceinline__ uint4 ld_u4(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
 
+// Asynchronous global -> shared copies (cp.async): a CTA issues all of its
+// small staging loads back to back and waits once.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+}
+
+// An always-zero value that the compiler cannot see through; adding it to an
+// address makes a later memory operation wait for the loads that produced x.
+__device__ __forceinline__ unsigned zero_dependent_on(unsigned x) {
+    unsigned z;
+    asm volatile("and.b32 %0, %1, 0;" : "=r"(z) : "r"(x));
+    return z;
+}
+
+// ---------------------------------------------------------------- mbarriers and bulk copies
+// Shared-memory transaction barriers and the bulk (TMA) copy engine, used by
+// the streaming pipeline.  Every wait is bounded: after kWaitLimitNs of
+// global time it gives up and returns false, so no launch can hang.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ unsigned smem_u32(const void *p) { return (unsigned)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, unsigned bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+                     smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Waits for the phase of the given parity to complete; false on time-out.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+// Bulk copy of `bytes` contiguous bytes global -> shared, completing on `bar`,
+// with an evict-first L2 policy (the checkpoint is read once per launch).
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, unsigned bytes, uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .b64 pol;\n\t"
+        "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], pol;\n\t}" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Named barrier over the first `count` threads of the CTA (the consumer
+// warps) that also ORs a flag over them: every participant gets the same
+// answer, so an abort decided on it is uniform and no thread is left waiting.
+__device__ __forceinline__ bool named_sync_or(int id, int count, bool flag) {
+    unsigned r;
+    asm volatile(
+        "{\n\t.reg .pred q, o;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred o, %2, %3, q;\n\tselp.u32 %0, 1, 0, o;\n\t}"
+        : "=r"(r)
+        : "r"((unsigned)flag), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 // ---------------------------------------------------------------- tile geometry
 // A (N x P) checkpoint slab is row-major with P contiguous.  A thread owns VEC
 // consecutive value columns (one 16-byte vector) of R consecutive key rows:
@@ -131,18 +224,6 @@ __device__ __forceinline__ void cta_reduce(float (&acc)[NV][VEC], int nv, float 
         red[i] = s;
     }
     __syncthreads();
-}
-
-// Per-sequence arrival: every CTA of sequence b calls this exactly once per
-// launch (thread 0, after the CTA has finished reading the pointers).
-// Returns true in the last CTA to arrive, which may then update the
-// sequence's pointers; the counter wraps back to 0 for the next launch.
-__device__ __forceinline__ bool arrive_last(uint32_t *counter, unsigned ctas_per_seq) {
-    __threadfence();
-    const unsigned prev = atomicInc(counter, ctas_per_seq - 1);
-    const bool last = prev == ctas_per_seq - 1;
-    if (last) __threadfence();
-    return last;
 }
 
 }  // namespace rs

@@ -29,7 +29,8 @@ def _run_standard(w, steps, seed=0, precision="fp32", sample=None, check_materia
         if folded:
             flushes += 1
             ck = rel_err(run.checkpoint(), run.model.S).max()
-            assert ck <= TOL_HP, f"step {s}: flushed checkpoint rel err {ck:.3e}"
+            tol_ck = TOL_LP if precision == "shared_bf16" else TOL_HP  # a bf16 checkpoint
+            assert ck <= tol_ck, f"step {s}: flushed checkpoint rel err {ck:.3e}"
             worst_ck = max(worst_ck, ck)
         if check_materialize:
             m = rel_err(run.materialized(), run.model.S).max()
