@@ -3,15 +3,19 @@
 
 A step is one standard decode step of the whole batch through the C ABI:
 append the step's record, replay the buffer against the checkpoint for the
-output, and (every L steps) fold the window into the checkpoint.  Workload:
-Mamba-2 layer, B=256 sequences, 128 heads, headdim 64, dstate 128, 8 B/C
-groups, window L=16, fp32 checkpoint (4 MiB per sequence), seeded synthetic
-inputs.  The timed region covers whole windows, so flushes are amortised.
+output, and (every L steps) fold the window into the checkpoint.  Headline
+workload: Mamba-2 layer, B=256 sequences, 128 heads, headdim 64, dstate 128,
+8 B/C groups, window L=16, fp32 checkpoint (4 MiB per sequence), seeded
+synthetic inputs.  The timed region covers whole windows, so flushes are
+amortised.
 
 Prints one JSON line: decode tokens/s (whole job), achieved HBM GB/s of the
 replay kernel against the measured peak, the eager load-update-store kernel
 on the same workload, an end-to-end number through host buffers, the fp64
-CPU oracle on a bounded sample, and the SM clocks seen while timing.
+CPU oracle on a bounded sample, the SM clocks seen while timing, and (unless
+--headline-only) the other workloads: GDN decode, Mamba-2 speculative
+verification, two-precision GDN speculative verification, each against its
+baseline kernel.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 Under torchrun every rank runs its own B sequences (weak scaling, no
@@ -29,13 +33,10 @@ import sys
 import tempfile
 import time
 
-import numpy as np
-
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "SSM-layer decode tokens/s at B=256, L=16 (1 GB300); achieved HBM GB/s vs peak"
-WORKLOAD = "mamba2"
 INPUT_POOL = 256  # distinct seeded input steps, cycled through the timed region
 
 
@@ -45,10 +46,13 @@ def parse():
     ap.add_argument("--steps", type=int, default=2048)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="librs", choices=["librs", "reference"])
+    ap.add_argument("--workload", default="mamba2", choices=["mamba2", "gdn"],
+                    help="decode workload of the headline line")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-eager", action="store_true")
+    ap.add_argument("--headline-only", action="store_true", help="skip the other workloads")
     ap.add_argument("--batch", type=int, default=0,
                     help="sequences per GPU (default: the workload's 256; smaller only for profiling)")
     return ap.parse_args()
@@ -75,10 +79,10 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic() -> float | None:
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (its source hash matches)."""
-    path = os.path.join(ROOT, "profiles", "replay_mamba2_traffic.json")
+def profiled_traffic(workload: str) -> float | None:
+    """DRAM bytes per launch (window average, full size) from the committed
+    ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"replay_{workload}_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
@@ -86,7 +90,7 @@ def profiled_traffic() -> float | None:
         return None
     if rec.get("source_hash") != kernel_source_hash():
         return None
-    return rec.get("dram_bytes_per_launch_full_size")
+    return rec.get("dram_bytes_per_launch")
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -109,7 +113,7 @@ class ClockSampler:
             self.proc = None
         time.sleep(0.3)
 
-    def stop(self) -> dict | None:
+    def stop(self):
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -136,7 +140,8 @@ class ClockSampler:
             if t0 - 0.06 <= ts <= t1 + 0.06:
                 sel.append(r)
         sel = sel or rows[-3:]
-        sm = [float(r[2]) for r in sel if r[2].strip().replace(".", "").isdigit()]
+        num = lambda v: v.strip().replace(".", "").isdigit()
+        sm = [float(r[2]) for r in sel if num(r[2])]
         reasons = set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in sel:
@@ -144,9 +149,9 @@ class ClockSampler:
                 if v.strip() == "Active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": float(sel[0][3]) if sel[0][3].strip().replace(".", "").isdigit() else None,
+                "sm_max_mhz": float(sel[0][3]) if num(sel[0][3]) else None,
                 "reasons": sorted(reasons), "samples": len(sel),
-                "power_w_max": max(float(r[4]) for r in sel if r[4].strip().replace(".", "").isdigit())}
+                "power_w_max": max([float(r[4]) for r in sel if num(r[4])] or [0.0])}
 
 
 # ----------------------------------------------------------------------------- ranks
@@ -191,8 +196,31 @@ def time_oracle(w, seconds: float, batch: int = 16):
                       f"(H={w.H}, P={w.P}, N={w.N}), fp64 eager recurrence, {el:.1f} s"}
 
 
-# ----------------------------------------------------------------------------- main arm
-def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
+# ----------------------------------------------------------------------------- GPU helpers
+def _events(n):
+    import torch
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def _params(w, dev):
+    import torch
+    from rs_decode_gb300 import synth
+    params = synth.layer_params(w)
+    if w.kind == "mamba2":
+        return params, {"A": torch.from_numpy(params["A"]).to(dev), "D": torch.from_numpy(params["D"]).to(dev)}
+    return params, {}
+
+
+def _init_state(layer, w, dev, seed):
+    import torch
+    g = torch.Generator(device=dev).manual_seed(1000 + seed)
+    S0 = torch.randn(layer.shape, generator=g, device=dev, dtype=torch.float32).mul_(w.init_std)
+    layer.init(S0)
+    return S0
+
+
+def measure_decode(w, K, W, dev, rank, world, want_eager=True, want_e2e=True, want_clocks=True):
+    """Standard decode of workload w: K timed steps after W warm-up steps."""
     import torch
     import torch.distributed as dist
 
@@ -200,22 +228,12 @@ def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
     from rs_decode_gb300 import synth, traffic
     from rs_decode_gb300.layer import Layer, to_device
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    w = synth.WORKLOADS[WORKLOAD]
-    if args.batch:
-        w = w.with_(B=args.batch)
-    K, W = args.steps, args.warmup
-    params = synth.layer_params(w)
-    gp = {"A": torch.from_numpy(params["A"]).to(dev), "D": torch.from_numpy(params["D"]).to(dev)}
+    params, gp = _params(w, dev)
     npool = min(INPUT_POOL, K + W)
     host_steps = [synth.step_inputs(w, s, seed=rank_seed(rank), params=params) for s in range(npool)]
     dev_steps = [to_device(d, dev) for d in host_steps]
-
-    layer = Layer("mamba2", w.B, w.H, w.G, w.P, w.N, w.L)
-    g = torch.Generator(device=dev).manual_seed(1000 + rank)
-    S0 = torch.randn(layer.shape, generator=g, device=dev, dtype=torch.float32).mul_(w.init_std)
-    layer.init(S0)
+    layer = Layer(w.kind, w.B, w.H, w.G, w.P, w.N, w.L)
+    S0 = _init_state(layer, w, dev, rank)
     y = torch.empty(w.B, w.H, w.P, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -223,15 +241,15 @@ def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
         if world > 1:
             dist.barrier()
 
-    # ---- replay path, device-resident inputs
     for s in range(W):
         layer.decode(dev_steps[s % npool], gp, y)
     torch.cuda.synchronize()
     h0 = int(layer.h[0].item())
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index or 0) if want_clocks else None
+    if clocks:
+        clocks.start()
+    ev = list(zip(_events(K), _events(K)))
+    start, end = _events(2)
     barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
@@ -244,50 +262,59 @@ def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
     torch.cuda.synchronize()
     t_wall1 = time.time()
     barrier()
-    rows = clocks.stop()
+    rows = clocks.stop() if clocks else None
     ms_total = start.elapsed_time(end)
     launch_ms = [a.elapsed_time(b) for a, b in ev]
     if layer.status() != 0:
         raise RuntimeError("device status bits set during the benchmark")
 
-    # algorithmic bytes of the timed launches (pointer schedule is lockstep)
-    shape = traffic.Shape("mamba2", w.B, w.H, w.G, w.P, w.N)
+    # algorithmic bytes of the timed launches (the pointer schedule is lockstep)
+    shape = traffic.Shape(w.kind, w.B, w.H, w.G, w.P, w.N)
     total_bytes, h = 0, h0
     for _ in range(K):
         flush = h + 1 >= w.L
         total_bytes += traffic.replay_step_bytes(shape, h, flush)
         h = 0 if flush else h + 1
 
-    # ---- eager baseline on the same workload
-    ms_eager = None
-    if not args.no_eager:
-        S_eager = S0.clone()
+    out = {"ms_total": ms_total, "ms_per_step": ms_total / K, "launch_ms": statistics.fmean(launch_ms),
+           "bytes_per_launch": total_bytes / K, "clock_rows": rows, "t_wall": (t_wall0, t_wall1),
+           "eager": None, "e2e": None}
+
+    if want_eager:
+        S_e = S0.clone()
         desc = layer.desc
         Ke = min(K, 512)
+
         def eager(s):
             d = dev_steps[s % npool]
-            rb.rs_eager_step_mamba2(desc, S_eager, d["x"], d["dt"], gp["A"], d["Bm"], d["Cm"], gp["D"], y)
+            if w.kind == "mamba2":
+                rb.rs_eager_step_mamba2(desc, S_e, d["x"], d["dt"], gp["A"], d["Bm"], d["Cm"], gp["D"], y)
+            else:
+                rb.rs_eager_step_gdn(desc, S_e, d["q"], d["k"], d["v"], d["alpha"], d["beta"], y)
         for s in range(W):
             eager(s)
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0, e1 = _events(2)
         e0.record(stream)
         for s in range(Ke):
             eager(W + s)
         e1.record(stream)
         torch.cuda.synchronize()
-        ms_eager = e0.elapsed_time(e1) / Ke
-        del S_eager
+        ms_e = e0.elapsed_time(e1) / Ke
+        eb = traffic.eager_step_bytes(shape)
+        out["eager"] = {"ms_per_step": ms_e, "value": w.B / (ms_e * 1e-3), "unit": "tokens/s",
+                        "achieved_gbs": eb / (ms_e * 1e-3) / 1e9, "bytes_per_step": eb,
+                        "speedup_of_replay": ms_e / (ms_total / K)}
+        del S_e
 
-    # ---- end to end through host buffers (pinned), copies inside the timed region
-    e2e = None
-    if not args.no_e2e:
+    if want_e2e:
         pinned = [{k: v.pin_memory() for k, v in to_device(d, "cpu").items()} for d in host_steps[:64]]
         stage = {k: torch.empty_like(v, device=dev) for k, v in pinned[0].items()}
         y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
         bi = sum(v.numel() * v.element_size() for v in pinned[0].values())
         bo = y.numel() * y.element_size()
         Kx = min(K, 512)
+
         def e2e_step(s):
             for k, v in pinned[s % len(pinned)].items():
                 stage[k].copy_(v, non_blocking=True)
@@ -296,7 +323,7 @@ def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
         for s in range(W):
             e2e_step(s)
         torch.cuda.synchronize()
-        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x0, x1 = _events(2)
         barrier()
         x0.record(stream)
         for s in range(Kx):
@@ -304,23 +331,148 @@ def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
         x1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        ms_x = x0.elapsed_time(x1) / Kx
-        e2e = {"value": w.B * world / (ms_x * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
-               "d2h_bytes_per_step": bo, "ms_per_step": ms_x}
+        ms_x = max_over_ranks(x0.elapsed_time(x1) / Kx, dev)
+        out["e2e"] = {"value": w.B * world / (ms_x * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
+                      "d2h_bytes_per_step": bo, "ms_per_step": ms_x}
+    del layer
+    torch.cuda.empty_cache()
+    return out
 
-    # ---- max over ranks
-    ms_total = max_over_ranks(ms_total, dev)
+
+def measure_spec(w, rounds, W, dev, rank):
+    """Speculative rounds of workload w (verify T drafts + commit) against the
+    per-draft snapshot baseline; committed and verified tokens/s and GB/s."""
+    import torch
+
+    from rs_decode_gb300 import binding as rb
+    from rs_decode_gb300 import synth, traffic
+    from rs_decode_gb300.layer import Layer, to_device
+
+    params, gp = _params(w, dev)
+    npool = 32
+    host = [synth.round_inputs(w, r, seed=rank_seed(rank), params=params) for r in range(npool)]
+    dev_rounds = [to_device(d, dev) for d in host]
+    prec = {"fp32": rb.PREC_FP32, "two": rb.PREC_TWO, "shared_bf16": rb.PREC_SHARED_BF16}[w.precision]
+    layer = Layer(w.kind, w.B, w.H, w.G, w.P, w.N, w.L, T_max=w.T, capacity=w.cap, precision=prec)
+    y = torch.empty(w.B, w.T, w.H, w.P, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def round_(r):
+        d = dev_rounds[r % npool]
+        layer.verify(w.T, d, gp, y)
+        layer.commit(d["accepted"])
+
+    # accounting pass: the committed counts before every round (the trajectory
+    # is deterministic, so the timed pass repeats it exactly)
+    S0 = _init_state(layer, w, dev, rank)
+    h_before = []
+    for r in range(W + rounds):
+        h_before.append(layer.h.cpu().numpy().copy())
+        round_(r)
+    layer.init(S0)
+    for r in range(W):
+        round_(r)
+    torch.cuda.synchronize()
+    e0, e1 = _events(2)
+    e0.record(stream)
+    for r in range(W, W + rounds):
+        round_(r)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / rounds
+    if layer.status() != 0:
+        raise RuntimeError("device status bits set during the speculative benchmark")
+    shape = traffic.Shape(w.kind, w.B, w.H, w.G, w.P, w.N)
+    two = w.precision == "two"
+    tot_bytes, folds, committed = 0, 0, 0
+    for r in range(W, W + rounds):
+        for hb in h_before[r]:
+            fold = traffic.spec_folds(int(hb), w.T, w.L)
+            folds += fold
+            rd = 4 if (fold or not two) else 2
+            wr = (6 if two else 4) if fold else 0
+            tot_bytes += traffic.verify_round_bytes(shape, w.T, int(hb), fold, rd, wr)
+        committed += int(host[r % npool]["accepted"].sum())
+    # baseline: per-draft snapshots (one state read + T state writes per round)
+    desc = layer.desc
+    del layer
+    torch.cuda.empty_cache()
+    pool = torch.empty(w.B, w.T + 1, w.H, w.N, w.P, device=dev)
+    pool[:, 0].copy_(S0)
+    del S0
+    cur = torch.zeros(w.B, dtype=torch.int32, device=dev)
+
+    def snap(r):
+        d = dev_rounds[r % npool]
+        ins = (rb.make_inputs(x=d["x"], dt=d["dt"], A=gp["A"], Bm=d["Bm"], Cm=d["Cm"], D=gp["D"])
+               if w.kind == "mamba2" else
+               rb.make_inputs(q=d["q"], k=d["k"], v=d["v"], alpha=d["alpha"], beta=d["beta"]))
+        rb.rs_eager_verify_snapshots(desc, pool, cur, w.T, ins, y)
+        rb.rs_eager_select(desc, cur, d["accepted"])
+    for r in range(W):
+        snap(r)
+    torch.cuda.synchronize()
+    b0, b1 = _events(2)
+    b0.record(stream)
+    for r in range(W, W + rounds):
+        snap(r)
+    b1.record(stream)
+    torch.cuda.synchronize()
+    ms_b = b0.elapsed_time(b1) / rounds
+    base_bytes = w.B * traffic.snapshot_round_bytes(shape, w.T)
+    del pool
+    torch.cuda.empty_cache()
+    per_round_committed = committed / rounds
+    return {"workload": f"{w.name}: {w.kind} B={w.B} H={w.H} G={w.G} P={w.P} N={w.N} L={w.L} T={w.T} "
+                        f"capacity={w.cap} accept={w.accept} precision={w.precision}",
+            "ms_per_round": ms, "committed_tokens_per_s": per_round_committed / (ms * 1e-3),
+            "verified_tokens_per_s": w.B * w.T / (ms * 1e-3),
+            "achieved_gbs": tot_bytes / rounds / (ms * 1e-3) / 1e9,
+            "bytes_per_round": tot_bytes / rounds, "fold_fraction": folds / (rounds * w.B),
+            "baseline": {"kind": "per-draft snapshots", "ms_per_round": ms_b,
+                         "committed_tokens_per_s": per_round_committed / (ms_b * 1e-3),
+                         "achieved_gbs": base_bytes / (ms_b * 1e-3) / 1e9, "bytes_per_round": base_bytes},
+            "speedup": ms_b / ms, "rounds": rounds, "launches_per_round": 2}
+
+
+# ----------------------------------------------------------------------------- main arm
+def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
+    import torch
+
+    from rs_decode_gb300 import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = synth.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(B=args.batch)
+    K, W = args.steps, args.warmup
+    m = measure_decode(w, K, W, dev, rank, world, want_eager=not args.no_eager, want_e2e=not args.no_e2e)
+    ms_total = max_over_ranks(m["ms_total"], dev)
+
+    peak = measured_peaks().get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or 6800.0
+    others = {}
+    if not args.headline_only and world == 1 and not args.batch:
+        other = "gdn" if w.kind == "mamba2" else "mamba2"
+        g = measure_decode(synth.WORKLOADS[other], 512, W, dev, rank, world, want_e2e=False, want_clocks=False)
+        gbs = g["bytes_per_launch"] / (g["launch_ms"] * 1e-3) / 1e9
+        others[other] = {"workload": f"{other} decode (shapes of the {other} workload), fp32 checkpoint",
+                         "value": 256 / (g["ms_per_step"] * 1e-3), "unit": "tokens/s",
+                         "ms_per_step": g["ms_per_step"], "achieved_gbs": gbs,
+                         "frac_of_measured_peak": gbs / peak, "eager": g["eager"]}
+        for name in ("mamba2_spec", "gdn_spec"):
+            o = measure_spec(synth.WORKLOADS[name], 64, 8, dev, rank)
+            o["frac_of_measured_peak"] = o["achieved_gbs"] / peak
+            others[name] = o
     if rank != 0:
         return None
 
-    peaks = measured_peaks()
-    peak = peaks.get("hbm_gbs")
-    peak_src = "measured" if peak else "fallback"
-    peak = peak or 6800.0
-    avg_launch_s = statistics.fmean(launch_ms) * 1e-3
-    achieved = total_bytes / K / avg_launch_s / 1e9
-    eager_bytes = traffic.eager_step_bytes(shape)
-    clk = ClockSampler.summarise(rows, t_wall0, t_wall1)
+    achieved = m["bytes_per_launch"] / (m["launch_ms"] * 1e-3) / 1e9
+    clk = ClockSampler.summarise(m["clock_rows"], *m["t_wall"]) if m["clock_rows"] else None
+    kernel = {"mamba2": "replay_pipe_kernel<mamba2, P=64, N=128, HU=8, TMAX=1, NC=256, NS=2>",
+              "gdn": "replay_pipe_kernel<gdn, P=128, N=128, HU=2, TMAX=1, NC=256, NS=2>"}[w.kind]
     out = {
         "metric": METRIC,
         "value": w.B * K * world / (ms_total * 1e-3),
@@ -334,25 +486,23 @@ def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": f"mamba2 decode B={w.B} H={w.H} P={w.P} N={w.N} G={w.G} L={w.L} fp32 checkpoint",
+        "config": {"workload": f"{w.kind} decode B={w.B} H={w.H} P={w.P} N={w.N} G={w.G} L={w.L} fp32 checkpoint",
                    "B_per_gpu": w.B, "window_L": w.L, "state_mib_per_seq": w.H * w.N * w.P * 4 / 2**20,
                    "parallelism": f"dp{world}" if world > 1 else "single",
                    "l2": "inputs larger than L2 (1 GiB checkpoint per step)",
-                   "inputs": f"{npool} distinct seeded steps cycled"},
+                   "inputs": f"{min(INPUT_POOL, K + W)} distinct seeded steps cycled"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": profiled_traffic(),
-                     "peak_source": f"{peak_src} (copy bandwidth)",
-                     "algorithmic_bytes_per_launch": total_bytes / K,
-                     "kernel": "replay_kernel<mamba2,64,128,HPC=2,TMAX=1,256>"},
+                     "frac": achieved / peak, "traffic": profiled_traffic(w.kind),
+                     "peak_source": f"{peak_src} (copy bandwidth, MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes_per_launch": m["bytes_per_launch"], "kernel": kernel},
         "hbm_gbs": achieved,
-        "eager": None if ms_eager is None else {
-            "ms_per_step": ms_eager, "value": w.B / (ms_eager * 1e-3), "unit": "tokens/s",
-            "achieved_gbs": eager_bytes / (ms_eager * 1e-3) / 1e9,
-            "bytes_per_step": eager_bytes, "speedup_of_replay": ms_eager / (ms_total / K)},
+        "eager": m["eager"],
         "gpu_launches": K,
         "clocks": clk,
-        "e2e": e2e,
+        "e2e": m["e2e"],
     }
+    if others:
+        out["workloads"] = others
     return out
 
 
@@ -363,12 +513,12 @@ def main():
         if rank != 0:
             return 0
         from rs_decode_gb300 import synth
-        w = synth.WORKLOADS[WORKLOAD]
+        w = synth.WORKLOADS[args.workload]
         ref = time_oracle(w, max(2.0, args.cpu_seconds))
         line = {"impl": "reference", "metric": METRIC, "value": ref["value"], "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": f"mamba2 decode B={w.B} H={w.H} P={w.P} N={w.N} G={w.G} L={w.L}"},
+                "config": {"workload": f"{w.kind} decode B={w.B} H={w.H} P={w.P} N={w.N} G={w.G} L={w.L}"},
                 "cpu_baseline": ref,
                 "e2e": {"value": ref["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
@@ -383,7 +533,7 @@ def main():
     if out is not None:
         if not args.no_cpu_baseline and world == 1:
             from rs_decode_gb300 import synth
-            out["cpu_baseline"] = time_oracle(synth.WORKLOADS[WORKLOAD], args.cpu_seconds)
+            out["cpu_baseline"] = time_oracle(synth.WORKLOADS[args.workload], args.cpu_seconds)
         print(json.dumps(out))
     if world > 1:
         import torch.distributed as dist

@@ -71,3 +71,9 @@ def verify_round_bytes(s: Shape, T: int, h_before: int, flush: bool, read_bytes:
 def snapshot_round_bytes(s: Shape, T: int) -> int:
     """Per-draft snapshot baseline, one sequence: read the state, write T states."""
     return s.state_elems * 4 * (1 + T) + T * (s.input_bytes + s.y_bytes)
+
+
+def spec_folds(h_before: int, T: int, L: int) -> bool:
+    """Whether a verify round starting with h_before committed records folds
+    them into the checkpoint (the library's rule: h + T > L and h > 0)."""
+    return h_before + T > L and h_before > 0
