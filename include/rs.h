@@ -59,7 +59,8 @@ typedef enum {
     RS_ERR_UNSUPPORTED = 2,  /* shape or mode without a kernel instantiation */
     RS_ERR_CAPACITY = 3,     /* capacity too small for L + T_max             */
     RS_ERR_CUDA = 4,         /* a CUDA call failed (launch or copy)          */
-    RS_ERR_DEVICE = 5        /* the device status word has bits set          */
+    RS_ERR_DEVICE = 5,       /* the device status word has bits set          */
+    RS_ERR_STATIC_LIMIT = 6  /* B above RS_STATIC_MAX_SEQS (rs_decode_mamba2_noalloc) */
 } rs_status;
 
 /* Bits of the device status word. */
@@ -224,6 +225,30 @@ rs_status rs_eager_verify_snapshots(const rs_layer_desc *desc, float *pool, cons
  * RS_DEV_ACCEPT for an accepted length outside 0..T_max. */
 rs_status rs_eager_select(const rs_layer_desc *desc, int32_t *cur, const int32_t *accepted,
                           uint32_t *status, void *stream);
+
+/* ------------------------------------------------- decode without caller scratch */
+/* Largest batch rs_decode_mamba2_noalloc accepts. */
+#define RS_STATIC_MAX_SEQS 4096
+
+/* rs_decode_mamba2 for callers that cannot give the library any device memory
+ * beyond inputs, outputs and the layer state (no counterpart in the paper: it
+ * is a packaging choice).  Examples are an engine plugin that only receives
+ * pre-planned tensors, or a server that forbids device allocation after
+ * start-up.  The per-sequence arrival counters, which rs_decode_mamba2 keeps in
+ * st->arrive (that member is ignored here and may be NULL), live in a 16 KiB
+ * static device array of this library instead.
+ *   - B <= RS_STATIC_MAX_SEQS, else RS_ERR_STATIC_LIMIT and nothing is enqueued.
+ *   - The first call on a device looks up the array's address with that device
+ *     current; make it before any stream capture.  Each call clears the
+ *     counters it uses on `stream`, then runs the same kernel as
+ *     rs_decode_mamba2 with the same results.
+ *   - All calls share the array: calls that overlap on the GPU race, so
+ *     serialise them.  The array stays allocated on every device that loaded
+ *     the library until the process exits.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+rs_status rs_decode_mamba2_noalloc(const rs_layer_desc *desc, const rs_state *st, const uint16_t *x,
+                                   const float *dt, const float *A, const uint16_t *Bm,
+                                   const uint16_t *Cm, const float *D, float *y, void *stream);
 
 #ifdef __cplusplus
 }

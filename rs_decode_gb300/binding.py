@@ -20,7 +20,8 @@ MAMBA2, GDN = 0, 1
 PREC_FP32, PREC_TWO, PREC_SHARED_BF16 = 0, 1, 2
 DEV_CAPACITY, DEV_ACCEPT, DEV_DRAFTS_PENDING = 0x1, 0x2, 0x4
 STATUS = {0: "RS_OK", 1: "RS_ERR_INVALID_ARG", 2: "RS_ERR_UNSUPPORTED", 3: "RS_ERR_CAPACITY",
-          4: "RS_ERR_CUDA", 5: "RS_ERR_DEVICE"}
+          4: "RS_ERR_CUDA", 5: "RS_ERR_DEVICE", 6: "RS_ERR_STATIC_LIMIT"}
+STATIC_MAX_SEQS = 4096
 
 _c_i32 = ctypes.c_int32
 _vp = ctypes.c_void_p
@@ -67,6 +68,7 @@ _SIGS = {
     "rs_eager_verify_snapshots": [ctypes.POINTER(LayerDesc), _vp, _vp, ctypes.c_int,
                                   ctypes.POINTER(Inputs), _vp, _vp],
     "rs_eager_select": [ctypes.POINTER(LayerDesc), _vp, _vp, _vp, _vp],
+    "rs_decode_mamba2_noalloc": [ctypes.POINTER(LayerDesc), ctypes.POINTER(State)] + [_vp] * 8,
 }
 _RESTYPE = {"rs_status_string": ctypes.c_char_p, "rs_version": ctypes.c_char_p}
 
@@ -216,3 +218,11 @@ def rs_eager_verify_snapshots(desc, pool, cur, T: int, inputs: Inputs, y, stream
 def rs_eager_select(desc, cur, accepted, status=None, stream=None):
     _check("rs_eager_select", load().rs_eager_select(ctypes.byref(desc), _ptr(cur), _ptr(accepted),
                                                      _ptr(status), _stream(stream)))
+
+
+def rs_decode_mamba2_noalloc(desc, state, x, dt, A, Bm, Cm, D, y, stream=None):
+    """rs_decode_mamba2 with the arrival counters in the library's static
+    device array (state.arrive is ignored); for callers that cannot allocate."""
+    _check("rs_decode_mamba2_noalloc", load().rs_decode_mamba2_noalloc(
+        ctypes.byref(desc), ctypes.byref(state), _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm),
+        _ptr(D), _ptr(y), _stream(stream)))

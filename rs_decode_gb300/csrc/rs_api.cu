@@ -95,6 +95,7 @@ const char *rs_status_string(rs_status s) {
         case RS_ERR_CAPACITY: return "buffer capacity below L + T_max";
         case RS_ERR_CUDA: return "CUDA error";
         case RS_ERR_DEVICE: return "device status bits set";
+        case RS_ERR_STATIC_LIMIT: return "batch above the static scratch limit (RS_STATIC_MAX_SEQS)";
     }
     return "unknown status";
 }
