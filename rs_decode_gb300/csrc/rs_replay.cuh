@@ -1,0 +1,790 @@
+// Output-only replay kernels of the ReplaySSM decode path (Mamba-2 and Gated
+// DeltaNet): standard decode with the flush route fused, speculative verify
+// with the fold of committed records fused, forced flush, and materialise.
+//
+// The state of one (sequence, head) is S = gamma * S_c + sum_r w_r v_r k_r^T
+// over the records r since the checkpoint S_c ("ReplaySSM: Cache SSM Inputs,
+// Not State", section "How it works").  A step reads the checkpoint once and
+// writes only outputs and the appended record; the checkpoint is rewritten
+// only by a fold (the "flush route").
+//
+// Kernel structure: a persistent, warp-specialised streaming pipeline.
+//   * Work unit = HU heads of one sequence that share one key group.
+//   * A producer warp (one elected lane) plans each unit from the sequence's
+//     pointers and streams the unit's checkpoint slabs (one per head, N x P,
+//     contiguous; SPLIT row blocks per slab) into a ring of NS shared-memory
+//     stages with bulk (TMA) copies that complete on mbarriers.  It runs
+//     ahead into the next unit while the consumers finish the current one.
+//   * NC consumer threads stage every small operand of the unit (buffered
+//     records, the step's keys / queries / values, per-head constants) with
+//     one batch of cp.async copies, compute the key.query dots and decay
+//     coefficients once per unit, then per head: dot the slab with the query
+//     (GDN: and key) vectors, reduce across warps, write the outputs (GDN:
+//     and the correction term u), and on a fold rewrite the slab as
+//     gamma S_c + (V diag(w)) K^T from the staged copy.  A stage is handed back
+//     to the producer as soon as it has been read for the last time.
+// Slabs are key-major ([N][P], value index contiguous): each consumer thread
+// owns VEC value columns of R consecutive key rows, so its dot products
+// accumulate locally and only a per-head cross-warp reduction is needed.
+//
+// Per-sequence pointers (base, h, nd) are read once per unit by the producer;
+// the last unit to have read them (an arrival counter) writes the new values,
+// so no second launch is needed.  Every wait is bounded: on a time-out the CTA
+// raises RS_DEV_TIMEOUT, drains its copies and returns.
+#pragma once
+
+#include "rs_common.cuh"
+#include "rs_internal.h"
+
+namespace rs {
+
+template <int KIND_, int P_, int N_, int HU_, int TMAX_, int NC_, int NS_, int SPLIT_>
+struct PipeCfg {
+    static constexpr int KIND = KIND_, P = P_, N = N_, HU = HU_, TMAX = TMAX_, NC = NC_, NS = NS_, SPLIT = SPLIT_;
+    static constexpr int NCW = NC / 32;                   // consumer warps
+    static constexpr int NT = NC + 32;                    // + one producer warp
+    static constexpr int JMAX = (KIND == RS_GDN ? 2 : 1) * TMAX;
+    static constexpr int NP = N / SPLIT;                  // key rows per stage
+    static constexpr int STAGE = NP * P * 4;              // bytes of one fp32 row block = one stage
+    static_assert(NS >= SPLIT, "a folding head keeps all its row blocks resident");
+    // registers sized so that two CTAs fit on an SM (the draft-heavy T=8 shape excepted)
+    static constexpr int MIN_BLOCKS = TMAX <= 4 ? 2 : 1;
+};
+
+// What one launch does to one sequence, from its pointers and the mode.
+struct SeqPlan {
+    int base, hc, ndr;
+    int T;       // records appended by this launch
+    int F;       // records folded into the checkpoint (0: none)
+    int fold, ok, append, work;
+    unsigned err;
+};
+
+// Shared-memory carve-up, byte offsets (16-byte aligned; stages first).
+struct PipeSmem {
+    int stages, bars, plans, abort, kraw, xr, ar, sr, cst, vb, bt, d1, d2, c1, c2, g1, g2, fw, gF, pre1, pre2, red,
+        total;
+};
+
+__host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
+
+template <class C>
+__host__ __device__ inline PipeSmem pipe_smem(int cap) {
+    constexpr int HU = C::HU, TMAX = C::TMAX, P = C::P, N = C::N;
+    constexpr bool GDN = C::KIND == RS_GDN;
+    PipeSmem s;
+    int o = 0;
+    s.stages = o; o += C::NS * C::STAGE;
+    s.bars = o;   o += al16((2 * C::NS + 4) * 8);
+    s.plans = o;  o += al16(2 * (int)sizeof(SeqPlan));
+    s.abort = o;  o += 16;
+    s.kraw = o;   o += al16((cap + TMAX) * N * 2);                  // bf16 keys (rows < cap), queries (cap + i)
+    s.xr = o;     o += al16(HU * cap * P * (GDN ? 4 : 2));          // Mamba-2 x bf16 / GDN u fp32 per record
+    s.ar = o;     o += al16(HU * cap * 4);                          // decays alpha_r
+    s.sr = o;     o += al16(HU * cap * 4);                          // Mamba-2 dt_r
+    s.cst = o;    o += al16(2 * HU * 4);                            // Mamba-2 A_h, D_h
+    s.vb = o;     o += GDN ? al16(TMAX * HU * P * 2) : 0;           // GDN drafts' v (bf16)
+    s.bt = o;     o += GDN ? al16(TMAX * HU * 4) : 0;               // GDN drafts' beta
+    s.d1 = o;     o += al16(cap * TMAX * 4);
+    s.d2 = o;     o += al16(cap * TMAX * 4);
+    s.c1 = o;     o += al16(HU * TMAX * cap * 4);
+    s.c2 = o;     o += al16(HU * TMAX * cap * 4);
+    s.g1 = o;     o += al16(HU * TMAX * 4);
+    s.g2 = o;     o += al16(HU * TMAX * 4);
+    s.fw = o;     o += al16(HU * cap * 4);
+    s.gF = o;     o += al16(HU * 4);
+    s.pre1 = o;   o += GDN ? al16(HU * TMAX * P * 4) : 0;
+    s.pre2 = o;   o += GDN ? al16(HU * TMAX * P * 4) : 0;
+    s.red = o;    o += al16(2 * C::NCW * C::JMAX * P * 4);          // double-buffered warp partials
+    s.total = o;
+    return s;
+}
+
+__device__ __forceinline__ SeqPlan plan_sequence(const ReplayParams &p, int b) {
+    SeqPlan s;
+    const int mode = p.mode, cap = p.cap, L = p.L;
+    s.base = p.base[b];
+    s.hc = p.h[b];
+    s.ndr = p.nd[b];
+    s.T = mode == MODE_DECODE ? 1 : (mode == MODE_VERIFY ? p.T : 0);
+    s.F = 0;
+    s.fold = 0;
+    s.append = 0;
+    s.err = 0;
+    // a pointer state outside the buffer (never produced by the library) is
+    // reported and the sequence left untouched rather than indexed with it
+    s.ok = s.base >= 0 && s.base < cap && s.hc >= 0 && s.hc <= cap && s.ndr >= 0 && s.ndr <= cap;
+    if (s.ok) {
+        if (mode == MODE_DECODE) {
+            if (s.ndr) s.err |= RS_DEV_DRAFTS_PENDING;
+            s.ok = s.hc + 1 <= cap;
+            s.F = s.hc + 1;
+            s.fold = s.F >= L;
+            s.append = !s.fold;  // a folded record never needs its buffer slot
+        } else if (mode == MODE_VERIFY) {
+            if (s.ndr) s.err |= RS_DEV_DRAFTS_PENDING;
+            s.ok = s.hc + s.T <= cap;
+            s.fold = s.hc + s.T > L && s.hc > 0;
+            s.F = s.fold ? s.hc : 0;
+            s.append = 1;
+        } else {  // flush / materialise: the committed records
+            s.F = s.hc;
+            s.fold = mode == MODE_FLUSH && s.hc > 0;
+        }
+    }
+    if (!s.ok) s.err |= RS_DEV_CAPACITY;
+    s.work = s.ok && (mode != MODE_FLUSH || s.fold);
+    return s;
+}
+
+// Called once per unit, by the thread that read the unit's pointers.  The
+// counter's address depends on the values read, so the increment cannot be
+// performed before those reads completed; the unit that sees the count reach
+// units_per_seq-1 is the last reader of sequence b and writes the new
+// pointers at once.  atomicInc wraps the counter back to 0 for the next launch.
+__device__ __forceinline__ void arrive_and_update(const ReplayParams &p, const SeqPlan &s, int b,
+                                                  unsigned units_per_seq, bool report) {
+    if (p.mode == MODE_MATERIALIZE) return;
+    if (report && s.err) atomicOr(p.status, s.err);
+    const unsigned z = zero_dependent_on((unsigned)(s.base ^ s.hc ^ s.ndr));
+    const unsigned prev = atomicInc(p.arrive + b + z, units_per_seq - 1);
+    if (prev != units_per_seq - 1 || !s.ok) return;
+    const int cap = p.cap;
+    if (p.mode == MODE_DECODE) {
+        if (s.fold) { p.base[b] = (s.base + s.F) % cap; p.h[b] = 0; }
+        else p.h[b] = s.hc + 1;
+        p.nd[b] = 0;
+    } else if (p.mode == MODE_VERIFY) {
+        if (s.fold) { p.base[b] = (s.base + s.hc) % cap; p.h[b] = 0; }
+        p.nd[b] = s.T;
+    } else if (s.fold) {  // flush
+        p.base[b] = (s.base + s.hc) % cap;
+        p.h[b] = 0;
+    }
+}
+
+// Two-precision: a folding sequence reads the fp32 copy, any other the bf16
+// copy; shared-bf16 has only the bf16 copy.
+__device__ __forceinline__ bool plan_reads_lp(const ReplayParams &p, const SeqPlan &s) {
+    return p.prec == RS_PREC_SHARED_BF16 ||
+           (p.prec == RS_PREC_TWO && !s.fold && (p.mode == MODE_DECODE || p.mode == MODE_VERIFY));
+}
+
+// mbarrier wait that also gives up as soon as another role of the CTA has
+// aborted (the flag lives in shared memory).
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, unsigned parity, volatile int *abort_flag,
+                                              uint32_t *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(status, RS_DEV_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// R consecutive bf16 values (16-byte aligned when R >= 8, 8-byte when R == 4) as fp32.
+template <int R>
+__device__ __forceinline__ void load_bf16_run(const uint16_t *src, float (&out)[R]) {
+    if constexpr (R % 8 == 0) {
+#pragma unroll
+        for (int c = 0; c < R / 8; ++c) {
+            float f[8];
+            unpack<uint16_t, 8>(ld_u4(src + 8 * c), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) out[8 * c + e] = f[e];
+        }
+    } else if constexpr (R == 4) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(src);
+        out[0] = bf2f(u.x & 0xffffu); out[1] = __uint_as_float(u.x & 0xffff0000u);
+        out[2] = bf2f(u.y & 0xffffu); out[3] = __uint_as_float(u.y & 0xffff0000u);
+    } else {
+#pragma unroll
+        for (int k = 0; k < R; ++k) out[k] = bf2f(src[k]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Producer: plan each unit, publish the plan, stream the unit's row blocks.
+template <class C>
+__device__ __forceinline__ void producer(const ReplayParams &p, uint8_t *sm, const PipeSmem &L, int units) {
+    constexpr int HU = C::HU, NS = C::NS, N = C::N, P = C::P, SPLIT = C::SPLIT;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + L.bars), *empty = full + NS;
+    uint64_t *pfull = empty + NS, *pempty = pfull + 2;
+    SeqPlan *plans = reinterpret_cast<SeqPlan *>(sm + L.plans);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
+    const unsigned upseq = p.H / HU;
+    int it = 0, pu = 0;
+    int u = blockIdx.x;
+    SeqPlan cur;
+    if (u < units) {
+        cur = plan_sequence(p, u / upseq);
+        arrive_and_update(p, cur, u / upseq, upseq, (u % upseq) == 0);
+    }
+    for (; u < units; u += gridDim.x, ++pu) {
+        const int b = u / upseq, h0 = (u % upseq) * HU;
+        if (!wait_or_abort(pempty + (pu & 1), ((pu >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        plans[pu & 1] = cur;
+        mbar_arrive(pfull + (pu & 1));  // release: the plan is visible to the consumers
+        const int un = u + gridDim.x;
+        SeqPlan next;
+        bool planned = false;
+        if (cur.work) {
+            const bool lp = plan_reads_lp(p, cur);
+            const unsigned slab = (unsigned)(N * P * (lp ? 2 : 4)), part = slab / SPLIT;
+            const uint8_t *src = (lp ? reinterpret_cast<const uint8_t *>(p.ckpt_lp)
+                                     : reinterpret_cast<const uint8_t *>(p.ckpt_hp)) +
+                                 ((size_t)b * p.H + h0) * slab;
+            bool stop = false;
+            for (int q = 0; q < HU * SPLIT; ++q, ++it) {
+                const int st = it % NS;
+                if (!wait_or_abort(empty + st, ((it / NS) & 1) ^ 1, abort_flag, p.status)) { stop = true; break; }
+                mbar_arrive_expect_tx(full + st, part);
+                bulk_copy_g2s(sm + L.stages + (size_t)st * C::STAGE, src + (size_t)q * part, part, full + st);
+                if (q == 0 && un < units) {  // plan the next unit while this one streams
+                    next = plan_sequence(p, un / upseq);
+                    arrive_and_update(p, next, un / upseq, upseq, (un % upseq) == 0);
+                    planned = true;
+                }
+            }
+            if (stop) break;
+        }
+        if (un < units && !planned) {
+            next = plan_sequence(p, un / upseq);
+            arrive_and_update(p, next, un / upseq, upseq, (un % upseq) == 0);
+        }
+        cur = next;
+    }
+    if (*abort_flag) {
+        // drain: wait (bounded) for the copies this thread may still have in flight
+        for (int k = it - NS > 0 ? it - NS : 0; k < it; ++k) mbar_wait(full + k % NS, (k / NS) & 1);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Fold of one staged row block: S_new = gF S_c + sum_{r<F} (fw_r v_r) k_r^T,
+// written to the checkpoint (both copies as present) or to the materialise
+// output.  The coefficient fw_r v_r of this thread's columns is formed once per
+// record and applied to all R rows the thread owns.
+template <class C, typename TE, int R, int VEC>
+__device__ __forceinline__ void fold_block(const ReplayParams &p, const TE *blk, const uint16_t *kraw,
+                                           const uint16_t *xb, const float *uf, const float *fw, float gf, int F,
+                                           int cap, int j, int row0, int n0p, int p0, size_t goff, bool materialize) {
+    constexpr int P = C::P, N = C::N;
+    float o[R][VEC];
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+        unpack<TE, VEC>(ld_u4(blk + (size_t)(n0p + k) * P + p0), o[k]);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) o[k][e] *= gf;
+    }
+    for (int r = 0; r < F; ++r) {
+        float cf[VEC];
+        const float w = fw[j * cap + r];
+        if constexpr (C::KIND == RS_MAMBA2) {
+            float xv[VEC];
+            load_bf16_run<VEC>(xb + ((size_t)j * cap + r) * P + p0, xv);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) cf[e] = w * xv[e];
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; e += 4) {
+                const float4 u4 = *reinterpret_cast<const float4 *>(uf + ((size_t)j * cap + r) * P + p0 + e);
+                cf[e] = w * u4.x; cf[e + 1] = w * u4.y; cf[e + 2] = w * u4.z; cf[e + 3] = w * u4.w;
+            }
+        }
+        float kr[R];
+        load_bf16_run<R>(kraw + (size_t)r * N + row0 + n0p, kr);
+#pragma unroll
+        for (int k = 0; k < R; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) o[k][e] = fmaf(cf[e], kr[k], o[k][e]);
+    }
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+        const size_t off = goff + (size_t)(row0 + n0p + k) * P + p0;
+        if (materialize) {
+            store_f32<VEC>(p.out + off, o[k]);
+        } else {
+            if (p.ckpt_hp) store_f32<VEC>(p.ckpt_hp + off, o[k]);
+            if (p.ckpt_lp) store_bf16<VEC>(p.ckpt_lp + off, o[k]);
+        }
+    }
+}
+
+// Consumers: everything but the slab stream.
+template <class C, typename TE>
+__device__ __forceinline__ bool consume_unit(const ReplayParams &p, uint8_t *sm, const PipeSmem &L, const SeqPlan &s,
+                                             const int b, const int h0, int &it) {
+    constexpr int KIND = C::KIND, P = C::P, N = C::N, HU = C::HU, TMAX = C::TMAX, NC = C::NC, NS = C::NS;
+    constexpr int JMAX = C::JMAX, NCW = C::NCW, SPLIT = C::SPLIT, NP = C::NP;
+    using Gm = Geo<P, NP, NC, TE>;
+    constexpr int VEC = Gm::VEC, TPR = Gm::TPR, R = Gm::R;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int H = p.H, G = p.G, cap = p.cap, mode = p.mode;
+    const int g = h0 / (H / G);
+    const int n0p = (tid / TPR) * R, p0 = (tid % TPR) * VEC;  // rows within a row block, columns
+    const int base = s.base, hc = s.hc, T = s.T, F = s.F;
+    const bool fold = s.fold, append = s.append, materialize = mode == MODE_MATERIALIZE;
+    const bool keep = fold || materialize;  // the staged slab is needed again after the reduction
+    const int J = (KIND == RS_GDN ? 2 : 1) * T;
+    const int nrec = hc + T;
+    auto slot = [&](int r) { return (base + r) % cap; };
+
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + L.bars), *empty = full + NS;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
+    uint16_t *kraw = reinterpret_cast<uint16_t *>(sm + L.kraw);
+    uint16_t *xb = reinterpret_cast<uint16_t *>(sm + L.xr);  // Mamba-2 x (bf16)
+    float *uf = reinterpret_cast<float *>(sm + L.xr);        // GDN u (fp32)
+    float *ar = reinterpret_cast<float *>(sm + L.ar), *sr = reinterpret_cast<float *>(sm + L.sr);
+    float *cst = reinterpret_cast<float *>(sm + L.cst);      // A_h (HU), D_h (HU)
+    uint16_t *vb = reinterpret_cast<uint16_t *>(sm + L.vb);
+    float *bt = reinterpret_cast<float *>(sm + L.bt);
+    float *d1 = reinterpret_cast<float *>(sm + L.d1), *d2 = reinterpret_cast<float *>(sm + L.d2);
+    float *c1 = reinterpret_cast<float *>(sm + L.c1), *c2 = reinterpret_cast<float *>(sm + L.c2);
+    float *g1 = reinterpret_cast<float *>(sm + L.g1), *g2 = reinterpret_cast<float *>(sm + L.g2);
+    float *fw = reinterpret_cast<float *>(sm + L.fw), *gF = reinterpret_cast<float *>(sm + L.gF);
+    float *pre1 = reinterpret_cast<float *>(sm + L.pre1), *pre2 = reinterpret_cast<float *>(sm + L.pre2);
+    float *red = reinterpret_cast<float *>(sm + L.red);
+
+    // ---- 1. one batch of cp.async copies for every small operand of the unit
+    {
+        constexpr int KC = N / 8;  // 16-byte chunks per key row
+        for (int i2 = tid; i2 < (nrec + T) * KC; i2 += NC) {
+            const int rr = i2 / KC, c = i2 % KC;
+            const uint16_t *src;
+            if (rr < hc) src = p.buf_k + (((size_t)b * cap + slot(rr)) * G + g) * N;
+            else if (rr < nrec) src = (KIND == RS_MAMBA2 ? p.Bm : p.k) + (((size_t)b * T + (rr - hc)) * G + g) * N;
+            else src = (KIND == RS_MAMBA2 ? p.Cm : p.q) + (((size_t)b * T + (rr - nrec)) * G + g) * N;
+            const int row = rr < nrec ? rr : cap + (rr - nrec);
+            cp_async16(kraw + (size_t)row * N + 8 * c, src + 8 * c);
+        }
+        if (KIND == RS_MAMBA2) {  // x of every record of the window, bf16
+            constexpr int XC = P / 8;
+            for (int i2 = tid; i2 < HU * nrec * XC; i2 += NC) {
+                const int c = i2 % XC, r = (i2 / XC) % nrec, hd = i2 / (XC * nrec), hh = h0 + hd;
+                const uint16_t *src = r < hc
+                    ? static_cast<const uint16_t *>(p.buf_v) + (((size_t)b * cap + slot(r)) * H + hh) * P
+                    : p.x + (((size_t)b * T + (r - hc)) * H + hh) * P;
+                cp_async16(xb + ((size_t)hd * cap + r) * P + 8 * c, src + 8 * c);
+            }
+            // A (forms the new records' decays) and D (the skip term of the
+            // outputs) only exist for launches that append records; flush and
+            // materialise pass neither
+            for (int i2 = tid; i2 < (T > 0 ? HU : 0); i2 += NC) {
+                cp_async4(cst + i2, p.A + h0 + i2);
+                if (p.D) cp_async4(cst + HU + i2, p.D + h0 + i2);
+                else cst[HU + i2] = 0.f;
+            }
+        } else {  // committed u (fp32); the drafts' v (bf16) and beta
+            constexpr int UC = P / 4, VC = P / 8;
+            for (int i2 = tid; i2 < HU * hc * UC; i2 += NC) {
+                const int c = i2 % UC, r = (i2 / UC) % hc, hd = i2 / (UC * hc), hh = h0 + hd;
+                const float *src = static_cast<const float *>(p.buf_v) + (((size_t)b * cap + slot(r)) * H + hh) * P;
+                cp_async16(uf + ((size_t)hd * cap + r) * P + 4 * c, src + 4 * c);
+            }
+            for (int i2 = tid; i2 < T * HU * VC; i2 += NC) {
+                const int c = i2 % VC, hd = (i2 / VC) % HU, i = i2 / (VC * HU);
+                cp_async16(vb + ((size_t)i * HU + hd) * P + 8 * c, p.v + (((size_t)b * T + i) * H + h0 + hd) * P + 8 * c);
+            }
+            for (int i2 = tid; i2 < T * HU; i2 += NC) {
+                const int hd = i2 % HU, i = i2 / HU;
+                cp_async4(bt + i2, p.beta + ((size_t)b * T + i) * H + h0 + hd);
+            }
+        }
+        for (int i2 = tid; i2 < HU * nrec; i2 += NC) {  // decays and value scales
+            const int r = i2 % nrec, hd = i2 / nrec, hh = h0 + hd;
+            if (r < hc) {
+                const size_t rec = ((size_t)b * cap + slot(r)) * H + hh;
+                cp_async4(ar + hd * cap + r, p.buf_a + rec);
+                if (KIND == RS_MAMBA2) cp_async4(sr + hd * cap + r, p.buf_s + rec);
+            } else {
+                const size_t bti = ((size_t)b * T + (r - hc)) * H + hh;
+                if (KIND == RS_MAMBA2) cp_async4(sr + hd * cap + r, p.dt + bti);
+                else cp_async4(ar + hd * cap + r, p.alpha + bti);
+            }
+        }
+        cp_async_wait_all();
+    }
+    if (named_sync_or(1, NC, false)) return false;
+
+    // ---- 2. new records' decays; appends
+    for (int i2 = tid; i2 < HU * T; i2 += NC) {
+        const int i = i2 / HU, hd = i2 % HU, hh = h0 + hd, r = hc + i;
+        float a;
+        if (KIND == RS_MAMBA2) {  // alpha = exp(dt A), formed once when the record is appended
+            a = expf(sr[hd * cap + r] * cst[hd]);
+            ar[hd * cap + r] = a;
+        } else {
+            a = ar[hd * cap + r];
+        }
+        if (append) {
+            const size_t rec = ((size_t)b * cap + slot(r)) * H + hh;
+            p.buf_a[rec] = a;
+            if (KIND == RS_MAMBA2) p.buf_s[rec] = sr[hd * cap + r];
+        }
+    }
+    if (append) {
+        if ((h0 % (H / G)) == 0) {  // the group's first unit appends the keys
+            for (int i2 = tid; i2 < T * (N / 8); i2 += NC) {
+                const int i = i2 / (N / 8), c = i2 % (N / 8);
+                uint16_t *dst = p.buf_k + (((size_t)b * cap + slot(hc + i)) * G + g) * N;
+                reinterpret_cast<uint4 *>(dst)[c] = reinterpret_cast<const uint4 *>(kraw + (size_t)(hc + i) * N)[c];
+            }
+        }
+        if (KIND == RS_MAMBA2) {
+            for (int i2 = tid; i2 < T * HU * (P / 8); i2 += NC) {
+                const int c = i2 % (P / 8), hd = (i2 / (P / 8)) % HU, i = i2 / ((P / 8) * HU);
+                uint16_t *dst = static_cast<uint16_t *>(p.buf_v) + (((size_t)b * cap + slot(hc + i)) * H + h0 + hd) * P;
+                reinterpret_cast<uint4 *>(dst)[c] = reinterpret_cast<const uint4 *>(xb + ((size_t)hd * cap + hc + i) * P)[c];
+            }
+        }
+    }
+
+    // ---- 3. key/query dot products of the group (8 lanes per dot)
+    if (T > 0) {
+        const int per = nrec * T;
+        const int ndots = (KIND == RS_GDN ? 2 : 1) * per;
+        for (int bd = 0; bd < ndots; bd += NC / 8) {
+            const int d = bd + tid / 8, sub = tid % 8;
+            float acc = 0.f;
+            int r = 0, i = 0, which = 0;
+            if (d < ndots) {
+                which = d / per;
+                r = (d % per) / T;
+                i = d % T;
+                const uint16_t *a = kraw + (size_t)r * N;
+                // Mamba-2: k_r . q_i ; GDN which 0: k_r . k_{hc+i}, which 1: k_r . q_i
+                const uint16_t *bv = (KIND == RS_GDN && which == 0) ? kraw + (size_t)(hc + i) * N
+                                                                    : kraw + (size_t)(cap + i) * N;
+                for (int n = sub * 8; n < N; n += 64) {
+                    float fa[8], fb[8];
+                    unpack<uint16_t, 8>(ld_u4(a + n), fa);
+                    unpack<uint16_t, 8>(ld_u4(bv + n), fb);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc = fmaf(fa[e], fb[e], acc);
+                }
+            }
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+            if (d < ndots && sub == 0) (which == 0 ? d1 : d2)[r * TMAX + i] = acc;
+        }
+    }
+    if (named_sync_or(1, NC, false)) return false;
+
+    // ---- 4. decay coefficients per head
+    // Record positions are 0-based; draft i sits at m_i = hc + i.  With
+    // E(r, m) = prod_{s=r+1..m} alpha_s and gamma(m) = prod_{s<=m} alpha_s:
+    //   Mamba-2  c1[i][r] = E(r, m_i) dt_r (k_r . q_i)   multiplies x_r[p] in y_i;  g1[i] = gamma(m_i)
+    //   GDN      c1[i][r] = E(r, m_i - 1) (k_r . k_{m_i})  (r < m_i)  -> S_{m_i - 1} k_{m_i}
+    //            c2[i][r] = E(r, m_i) (k_r . q_i)          (r <= m_i) -> S_{m_i} q_i
+    //            g1[i] = gamma(m_i - 1), g2[i] = gamma(m_i)
+    //   fold of F records: fw[r] = E(r, F-1) (times dt_r for Mamba-2), gF = gamma(F-1)
+    {
+        const int nA = HU * T * nrec;
+        for (int i2 = tid; i2 < nA + HU * T + HU * F + HU; i2 += NC) {
+            if (i2 < nA) {
+                const int r = i2 % nrec, i = (i2 / nrec) % T, hd = i2 / (nrec * T);
+                const float *a = ar + hd * cap;
+                const int m = hc + i;
+                float e = 1.f;  // E(r, m - 1)
+                for (int q = r + 1; q <= m - 1; ++q) e *= a[q];
+                const float em = r == m ? 1.f : e * a[m];  // E(r, m)
+                float v1 = 0.f, v2 = 0.f;
+                if (KIND == RS_MAMBA2) {
+                    if (r <= m) v1 = em * sr[hd * cap + r] * d1[r * TMAX + i];
+                } else {
+                    if (r < m) v1 = e * d1[r * TMAX + i];
+                    if (r <= m) v2 = em * d2[r * TMAX + i];
+                }
+                c1[(hd * TMAX + i) * cap + r] = v1;
+                c2[(hd * TMAX + i) * cap + r] = v2;
+            } else if (i2 < nA + HU * T) {
+                const int j = i2 - nA, i = j % T, hd = j / T;
+                const float *a = ar + hd * cap;
+                const int m = hc + i;
+                float e = 1.f;
+                for (int q = 0; q < m; ++q) e *= a[q];
+                g1[hd * TMAX + i] = KIND == RS_MAMBA2 ? e * a[m] : e;
+                g2[hd * TMAX + i] = e * a[m];
+            } else if (i2 < nA + HU * T + HU * F) {
+                const int j = i2 - nA - HU * T, r = j % F, hd = j / F;
+                const float *a = ar + hd * cap;
+                float e = 1.f;
+                for (int q = r + 1; q < F; ++q) e *= a[q];
+                fw[hd * cap + r] = KIND == RS_MAMBA2 ? e * sr[hd * cap + r] : e;
+            } else {
+                const int hd = i2 - nA - HU * T - HU * F;
+                const float *a = ar + hd * cap;
+                float e = 1.f;
+                for (int q = 0; q < F; ++q) e *= a[q];
+                gF[hd] = e;
+            }
+        }
+    }
+    if (named_sync_or(1, NC, false)) return false;
+
+    // ---- 5 (GDN): committed-record parts of S_{m_i-1} k_{m_i} and S_{m_i} q_i
+    if (KIND == RS_GDN && T > 0) {
+        for (int i2 = tid; i2 < HU * T * P; i2 += NC) {
+            const int pp = i2 % P, i = (i2 / P) % T, hd = i2 / (P * T);
+            float s1 = 0.f, s2 = 0.f;
+            for (int r = 0; r < hc; ++r) {
+                const float u = uf[((size_t)hd * cap + r) * P + pp];
+                s1 = fmaf(c1[(hd * TMAX + i) * cap + r], u, s1);
+                s2 = fmaf(c2[(hd * TMAX + i) * cap + r], u, s2);
+            }
+            pre1[(hd * TMAX + i) * P + pp] = s1;
+            pre2[(hd * TMAX + i) * P + pp] = s2;
+        }
+        // read after the first head's partial barrier
+    }
+
+    // ---- 6. the unit's heads: SPLIT ring stages each
+    for (int j = 0; j < HU; ++j) {
+        const int hh = h0 + j, it0 = it;
+        const size_t goff = ((size_t)b * H + hh) * ((size_t)N * P);
+        float acc[JMAX][VEC];
+#pragma unroll
+        for (int a = 0; a < JMAX; ++a)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) acc[a][e] = 0.f;
+        bool ok = true;
+        for (int part = 0; part < SPLIT; ++part, ++it) {
+            const int st = it % NS;
+            ok = wait_or_abort(full + st, (it / NS) & 1, abort_flag, p.status) && ok;
+            const TE *blk = reinterpret_cast<const TE *>(sm + L.stages + (size_t)st * C::STAGE);
+            if (ok && J > 0) {
+                const int row0 = part * NP + n0p;
+#pragma unroll
+                for (int k = 0; k < R; ++k) {
+                    float sv[VEC];
+                    unpack<TE, VEC>(ld_u4(blk + (size_t)(n0p + k) * P + p0), sv);
+#pragma unroll
+                    for (int jj = 0; jj < JMAX; ++jj) {
+                        if (jj < J) {
+                            // Mamba-2: q_jj ; GDN: jj < T -> k_{hc+jj}, else q_{jj-T}
+                            const int row = (KIND == RS_GDN && jj < T) ? hc + jj
+                                                                       : cap + (KIND == RS_GDN ? jj - T : jj);
+                            const float w = bf2f(kraw[(size_t)row * N + row0 + k]);
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e) acc[jj][e] = fmaf(sv[e], w, acc[jj][e]);
+                        }
+                    }
+                }
+            }
+            if (!keep) {  // last read of this row block: hand the stage back
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty + st);
+            }
+        }
+        // intra-warp reduction over the row groups of the warp, then per-warp partials
+#pragma unroll
+        for (int off = TPR; off < 32; off <<= 1)
+#pragma unroll
+            for (int a = 0; a < JMAX; ++a)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) acc[a][e] += __shfl_xor_sync(0xffffffffu, acc[a][e], off);
+        float *rb = red + (size_t)(j & 1) * NCW * JMAX * P;
+        if (lane < TPR) {
+#pragma unroll
+            for (int a = 0; a < JMAX; ++a)
+                if (a < J)
+#pragma unroll
+                    for (int c = 0; c < VEC / 4; ++c)
+                        reinterpret_cast<float4 *>(rb + ((size_t)warp * JMAX + a) * P + p0)[c] =
+                            make_float4(acc[a][4 * c], acc[a][4 * c + 1], acc[a][4 * c + 2], acc[a][4 * c + 3]);
+        }
+
+        if (KIND == RS_MAMBA2 && keep && ok) {  // the Mamba-2 fold needs nothing the reduction produces
+            for (int part = 0; part < SPLIT; ++part) {
+                const int st = (it0 + part) % NS;
+                fold_block<C, TE, R, VEC>(p, reinterpret_cast<const TE *>(sm + L.stages + (size_t)st * C::STAGE),
+                                          kraw, xb, uf, fw, gF[j], F, cap, j, part * NP, n0p, p0, goff, materialize);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty + st);
+            }
+        }
+        if (named_sync_or(1, NC, !ok)) return false;  // partials of head j complete
+
+        if (KIND == RS_MAMBA2) {
+            // y_i[p] = gamma(m_i) (S_c q_i)[p] + sum_r c1[i][r] x_r[p] + D x_{m_i}[p]
+            for (int i2 = tid; i2 < T * P; i2 += NC) {
+                const int i = i2 / P, pp = i2 % P, m = hc + i;
+                float sq = 0.f;
+#pragma unroll
+                for (int w = 0; w < NCW; ++w) sq += rb[((size_t)w * JMAX + i) * P + pp];
+                float yv = g1[j * TMAX + i] * sq;
+                const float *cc = c1 + (j * TMAX + i) * cap;
+                const uint16_t *xr = xb + (size_t)j * cap * P + pp;
+                for (int r = 0; r <= m; ++r) yv = fmaf(cc[r], bf2f(xr[(size_t)r * P]), yv);
+                yv = fmaf(cst[HU + j], bf2f(xr[(size_t)m * P]), yv);
+                p.y[(((size_t)b * T + i) * H + hh) * P + pp] = yv;
+            }
+        } else {
+            // GDN: per value index, the recurrence over the drafts
+            for (int pp = tid; pp < P; pp += NC) {
+                float ud[TMAX];
+#pragma unroll
+                for (int i = 0; i < TMAX; ++i) {
+                    ud[i] = 0.f;
+                    if (i < T) {
+                        const int m = hc + i;
+                        float ak = 0.f, bq = 0.f;  // (S_c k_{m_i})[p], (S_c q_i)[p]
+#pragma unroll
+                        for (int w = 0; w < NCW; ++w) {
+                            ak += rb[((size_t)w * JMAX + i) * P + pp];
+                            bq += rb[((size_t)w * JMAX + T + i) * P + pp];
+                        }
+                        float sk = g1[j * TMAX + i] * ak + pre1[(j * TMAX + i) * P + pp];
+                        const float *cc1 = c1 + (j * TMAX + i) * cap + hc;
+#pragma unroll
+                        for (int i3 = 0; i3 < TMAX; ++i3)
+                            if (i3 < i) sk = fmaf(cc1[i3], ud[i3], sk);
+                        const float u = bt[i * HU + j] * (bf2f(vb[((size_t)i * HU + j) * P + pp]) - ar[j * cap + m] * sk);
+                        ud[i] = u;
+                        uf[((size_t)j * cap + m) * P + pp] = u;
+                        if (append) static_cast<float *>(p.buf_v)[(((size_t)b * cap + slot(m)) * H + hh) * P + pp] = u;
+                        float yv = g2[j * TMAX + i] * bq + pre2[(j * TMAX + i) * P + pp];
+                        const float *cc2 = c2 + (j * TMAX + i) * cap + hc;
+#pragma unroll
+                        for (int i3 = 0; i3 < TMAX; ++i3)
+                            if (i3 <= i) yv = fmaf(cc2[i3], ud[i3], yv);
+                        p.y[(((size_t)b * T + i) * H + hh) * P + pp] = yv;
+                    }
+                }
+            }
+            if (keep) {
+                if (named_sync_or(1, NC, false)) return false;  // the new record's u is in uf
+                for (int part = 0; part < SPLIT; ++part) {
+                    const int st = (it0 + part) % NS;
+                    fold_block<C, TE, R, VEC>(p, reinterpret_cast<const TE *>(sm + L.stages + (size_t)st * C::STAGE),
+                                              kraw, xb, uf, fw, gF[j], F, cap, j, part * NP, n0p, p0, goff,
+                                              materialize);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(empty + st);
+                }
+            }
+        }
+    }
+    // the next unit's staging overwrites shared operands still read above
+    return !named_sync_or(1, NC, false);
+}
+
+template <class C>
+__device__ __forceinline__ void consumer(const ReplayParams &p, uint8_t *sm, const PipeSmem &L, int units) {
+    uint64_t *pfull = reinterpret_cast<uint64_t *>(sm + L.bars) + 2 * C::NS, *pempty = pfull + 2;
+    SeqPlan *plans = reinterpret_cast<SeqPlan *>(sm + L.plans);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
+    const unsigned upseq = p.H / C::HU;
+    int it = 0, pu = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++pu) {
+        const bool ok = wait_or_abort(pfull + (pu & 1), (pu >> 1) & 1, abort_flag, p.status);
+        SeqPlan s;
+        if (ok) s = plans[pu & 1];
+        if (named_sync_or(1, C::NC, !ok)) return;
+        if (threadIdx.x == 0) mbar_arrive(pempty + (pu & 1));
+        if (!s.work) continue;
+        const int b = u / upseq, h0 = (u % upseq) * C::HU;
+        const bool done = plan_reads_lp(p, s) ? consume_unit<C, uint16_t>(p, sm, L, s, b, h0, it)
+                                              : consume_unit<C, float>(p, sm, L, s, b, h0, it);
+        if (!done) return;
+    }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::NT, C::MIN_BLOCKS) replay_pipe_kernel(const ReplayParams p, int units) {
+    extern __shared__ __align__(128) uint8_t sm[];
+    const PipeSmem L = pipe_smem<C>(p.cap);
+    if (threadIdx.x == 0) {
+        uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bars);
+        for (int s = 0; s < C::NS; ++s) {
+            mbar_init(bars + s, 1);                 // full: the producer's expect_tx arrival
+            mbar_init(bars + C::NS + s, C::NCW);    // empty: one arrival per consumer warp
+        }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(bars + 2 * C::NS + k, 1);     // plan full
+            mbar_init(bars + 2 * C::NS + 2 + k, 1); // plan empty
+        }
+        *reinterpret_cast<volatile int *>(sm + L.abort) = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x >= C::NC) {
+        if (threadIdx.x == C::NC) producer<C>(p, sm, L, units);
+        return;
+    }
+    consumer<C>(p, sm, L, units);
+}
+
+// ---------------------------------------------------------------------------
+template <class C>
+cudaError_t launch_pipe(const ReplayParams &p, cudaStream_t stream) {
+    const PipeSmem L = pipe_smem<C>(p.cap);
+    const int smem = L.total;
+    auto kern = replay_pipe_kernel<C>;
+    static int smem_set = 0;  // largest opt-in already granted to this instantiation
+    static int per_sm = 0;
+    if (smem > smem_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        smem_set = smem;
+        per_sm = 0;
+    }
+    if (per_sm == 0) {
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::NT, smem);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    }
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int units = p.B * (p.H / C::HU);
+    const int grid = units < sms * per_sm ? units : sms * per_sm;
+    kern<<<grid, C::NT, smem, stream>>>(p, units);
+    return cudaGetLastError();
+}
+
+// Launch shapes.  Candidates are tried in order; the first whose heads per
+// unit divide the group and whose shared memory fits two CTAs on an SM wins,
+// else the first that fits one CTA.
+constexpr int kMaxSmemPerBlock = 227 * 1024;
+constexpr int kTwoPerSm = kMaxSmemPerBlock / 2 - 1024;
+
+template <class C>
+bool try_shape(const ReplayParams &p, int hpg, int limit, cudaStream_t s, cudaError_t &err) {
+    if (hpg % C::HU != 0 || pipe_smem<C>(p.cap).total > limit) return false;
+    err = launch_pipe<C>(p, s);
+    return true;
+}
+
+template <int KIND, int P, int N, int NC, int TMAX, int SPLIT, int NS, int... HUS>
+cudaError_t launch_shape(const ReplayParams &p, cudaStream_t s) {
+    const int hpg = p.H / p.G;
+    cudaError_t e = cudaErrorInvalidValue;
+    for (const int limit : {kTwoPerSm, kMaxSmemPerBlock})
+        if ((try_shape<PipeCfg<KIND, P, N, HUS, TMAX, NC, NS, SPLIT>>(p, hpg, limit, s, e) || ...)) return e;
+    return cudaErrorInvalidConfiguration;
+}
+
+// Verify launches instantiate the draft-count buckets 1, 4 and 8.
+template <int KIND, int P, int N, int NC, int SPLIT, int NS, int... HUS>
+cudaError_t dispatch_shape(const ReplayParams &p, cudaStream_t s) {
+    const int T = p.mode == MODE_VERIFY ? p.T : 1;
+    if (T <= 1) return launch_shape<KIND, P, N, NC, 1, SPLIT, NS, HUS...>(p, s);
+    if (T <= 4) return launch_shape<KIND, P, N, NC, 4, SPLIT, NS, HUS...>(p, s);
+    return launch_shape<KIND, P, N, NC, 8, SPLIT, NS, HUS...>(p, s);
+}
+
+// One translation unit per family / slab shape (compiled in parallel).
+cudaError_t replay_launch_m2_64x128(const ReplayParams &p, cudaStream_t s);
+cudaError_t replay_launch_gdn_128x128(const ReplayParams &p, cudaStream_t s);
+cudaError_t replay_launch_64x64(const ReplayParams &p, int kind, cudaStream_t s);
+
+}  // namespace rs
