@@ -53,6 +53,11 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-eager", action="store_true")
     ap.add_argument("--headline-only", action="store_true", help="skip the other workloads")
+    ap.add_argument("--spec", default="", choices=["", "mamba2_spec", "gdn_spec"],
+                    help="time only this speculative workload (verify + commit rounds) and print its line")
+    ap.add_argument("--rounds", type=int, default=64)
+    ap.add_argument("--sweep", action="store_true",
+                    help="print one JSON line per point of the window / batch / draft-count sweeps instead")
     ap.add_argument("--batch", type=int, default=0,
                     help="sequences per GPU (default: the workload's 256; smaller only for profiling)")
     return ap.parse_args()
@@ -232,7 +237,8 @@ def measure_decode(w, K, W, dev, rank, world, want_eager=True, want_e2e=True, wa
     npool = min(INPUT_POOL, K + W)
     host_steps = [synth.step_inputs(w, s, seed=rank_seed(rank), params=params) for s in range(npool)]
     dev_steps = [to_device(d, dev) for d in host_steps]
-    layer = Layer(w.kind, w.B, w.H, w.G, w.P, w.N, w.L)
+    prec = {"fp32": rb.PREC_FP32, "two": rb.PREC_TWO, "shared_bf16": rb.PREC_SHARED_BF16}[w.precision]
+    layer = Layer(w.kind, w.B, w.H, w.G, w.P, w.N, w.L, capacity=w.cap, precision=prec)
     S0 = _init_state(layer, w, dev, rank)
     y = torch.empty(w.B, w.H, w.P, device=dev)
     stream = torch.cuda.current_stream()
@@ -271,9 +277,12 @@ def measure_decode(w, K, W, dev, rank, world, want_eager=True, want_e2e=True, wa
     # algorithmic bytes of the timed launches (the pointer schedule is lockstep)
     shape = traffic.Shape(w.kind, w.B, w.H, w.G, w.P, w.N)
     total_bytes, h = 0, h0
+    two = w.precision == "two"
     for _ in range(K):
         flush = h + 1 >= w.L
-        total_bytes += traffic.replay_step_bytes(shape, h, flush)
+        rd = 4 if (flush or not two) else 2          # two-precision: bf16 copy off the flush steps
+        wr = 6 if two else 4                          # a fold writes both copies
+        total_bytes += traffic.replay_step_bytes(shape, h, flush, rd, wr)
         h = 0 if flush else h + 1
 
     out = {"ms_total": ms_total, "ms_per_step": ms_total / K, "launch_ms": statistics.fmean(launch_ms),
@@ -435,6 +444,39 @@ def measure_spec(w, rounds, W, dev, rank):
             "speedup": ms_b / ms, "rounds": rounds, "launches_per_round": 2}
 
 
+# ----------------------------------------------------------------------------- sweeps
+def run_sweeps(dev):
+    """Window size L, batch B, draft count T and two-precision sweeps of the
+    Mamba-2 serving layer (the pages' window trade-off and small-batch remark,
+    "ReplaySSM: Cache SSM Inputs, Not State", sections "How it works" and
+    "Limits"), each point against its baseline kernel."""
+    from rs_decode_gb300 import synth
+    peak = measured_peaks().get("hbm_gbs") or 6800.0
+    base = synth.WORKLOADS["mamba2"]
+
+    def dec(w, K=256):
+        m = measure_decode(w, K, 2 * w.L, dev, 0, 1, want_e2e=False, want_clocks=False)
+        gbs = m["bytes_per_launch"] / (m["launch_ms"] * 1e-3) / 1e9
+        return {"tokens_per_s": w.B / (m["ms_per_step"] * 1e-3), "achieved_gbs": gbs, "frac": gbs / peak,
+                "eager_tokens_per_s": m["eager"]["value"], "speedup_vs_eager": m["eager"]["speedup_of_replay"]}
+
+    for L in (8, 16, 32):
+        print(json.dumps({"sweep": "window", "L": L, "B": 256, **dec(base.with_(L=L), K=16 * L)}), flush=True)
+    for B in (1, 8, 32, 128, 512):
+        print(json.dumps({"sweep": "batch", "L": 16, "B": B, **dec(base.with_(B=B))}), flush=True)
+    print(json.dumps({"sweep": "precision", "precision": "two", "B": 256, "L": 16,
+                      **dec(base.with_(precision="two"))}), flush=True)
+    spec = synth.WORKLOADS["mamba2_spec"]
+    for T in (1, 2, 4, 8):
+        o = measure_spec(spec.with_(T=T, capacity=16 + T), 64, 8, dev, 0)
+        print(json.dumps({"sweep": "drafts", "T": T, "B": 256, "L": 16,
+                          "verified_tokens_per_s": o["verified_tokens_per_s"],
+                          "committed_tokens_per_s": o["committed_tokens_per_s"],
+                          "achieved_gbs": o["achieved_gbs"], "frac": o["achieved_gbs"] / peak,
+                          "snapshot_committed_tokens_per_s": o["baseline"]["committed_tokens_per_s"],
+                          "speedup_vs_snapshots": o["speedup"]}), flush=True)
+
+
 # ----------------------------------------------------------------------------- main arm
 def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
     import torch
@@ -526,6 +568,20 @@ def main():
         return 0
 
     import torch
+    if args.sweep:
+        torch.cuda.set_device(local_rank)
+        run_sweeps(torch.device("cuda", local_rank))
+        return 0
+    if args.spec:
+        from rs_decode_gb300 import synth
+        torch.cuda.set_device(local_rank)
+        w = synth.WORKLOADS[args.spec]
+        if args.batch:
+            w = w.with_(B=args.batch)
+        o = measure_spec(w, args.rounds, args.warmup, torch.device("cuda", local_rank), rank)
+        o["frac_of_measured_peak"] = o["achieved_gbs"] / (measured_peaks().get("hbm_gbs") or 6800.0)
+        print(json.dumps(o))
+        return 0
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))

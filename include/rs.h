@@ -126,6 +126,9 @@ typedef struct {
 /* ------------------------------------------------------------------- host-only */
 const char *rs_status_string(rs_status s);
 const char *rs_version(void);
+/* Name and text of the CUDA error behind the calling thread's most recent
+ * RS_ERR_CUDA ("" if none); for diagnostics. */
+const char *rs_last_cuda_error(void);
 
 /* Validates the descriptor and fills the array sizes.  Host only. */
 rs_status rs_state_bytes_for(const rs_layer_desc *desc, rs_state_bytes *out);

@@ -50,6 +50,7 @@ class Inputs(ctypes.Structure):
 _SIGS = {
     "rs_status_string": [ctypes.c_int],
     "rs_version": [],
+    "rs_last_cuda_error": [],
     "rs_state_bytes_for": [ctypes.POINTER(LayerDesc), ctypes.POINTER(StateBytes)],
     "rs_init": [ctypes.POINTER(LayerDesc), ctypes.POINTER(State), _vp, _vp],
     "rs_get_status": [ctypes.POINTER(State), ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, _vp],
@@ -70,7 +71,8 @@ _SIGS = {
     "rs_eager_select": [ctypes.POINTER(LayerDesc), _vp, _vp, _vp, _vp],
     "rs_decode_mamba2_noalloc": [ctypes.POINTER(LayerDesc), ctypes.POINTER(State)] + [_vp] * 8,
 }
-_RESTYPE = {"rs_status_string": ctypes.c_char_p, "rs_version": ctypes.c_char_p}
+_RESTYPE = {"rs_status_string": ctypes.c_char_p, "rs_version": ctypes.c_char_p,
+            "rs_last_cuda_error": ctypes.c_char_p}
 
 _lib = None
 
@@ -119,7 +121,10 @@ def _stream(stream) -> int | None:
 
 def _check(fn: str, status: int) -> None:
     if status != 0:
-        raise RsError(fn, status)
+        err = RsError(fn, status)
+        if status == 4:  # RS_ERR_CUDA: say which CUDA error
+            err.args = (f"{err.args[0]}: {load().rs_last_cuda_error().decode()}",)
+        raise err
 
 
 def make_desc(kind: int, B: int, H: int, G: int, P: int, N: int, L: int, T_max: int = 0,

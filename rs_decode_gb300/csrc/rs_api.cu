@@ -2,6 +2,7 @@
 // two kernel launches on the caller's stream.  No entry point allocates
 // memory or keeps state between calls.
 #include <stdint.h>
+#include <stdio.h>
 
 #include <cuda_runtime.h>
 
@@ -42,7 +43,13 @@ rs_status check_state(const rs_layer_desc *d, const rs_state *s) {
     return RS_OK;
 }
 
-rs_status cuda_status(cudaError_t e) { return e == cudaSuccess ? RS_OK : RS_ERR_CUDA; }
+thread_local char g_last_cuda_error[160] = "";
+
+rs_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return RS_OK;
+    snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return RS_ERR_CUDA;
+}
 
 ReplayParams replay_params(const rs_layer_desc *d, const rs_state *s, int mode, int T) {
     ReplayParams p = {};
@@ -101,6 +108,8 @@ const char *rs_status_string(rs_status s) {
 }
 
 const char *rs_version(void) { return "librs 0.1 (sm_103a)"; }
+
+const char *rs_last_cuda_error(void) { return g_last_cuda_error; }
 
 rs_status rs_state_bytes_for(const rs_layer_desc *d, rs_state_bytes *o) {
     RS_TRY(check_desc(d));

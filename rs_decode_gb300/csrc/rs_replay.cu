@@ -5,8 +5,8 @@
 namespace rs {
 
 cudaError_t replay_launch_64x64(const ReplayParams &p, int kind, cudaStream_t s) {
-    if (kind == RS_MAMBA2) return dispatch_shape<RS_MAMBA2, 64, 64, 128, 1, 2, 2, 1>(p, s);
-    return dispatch_shape<RS_GDN, 64, 64, 128, 1, 2, 2, 1>(p, s);
+    if (kind == RS_MAMBA2) return dispatch_shape<RS_MAMBA2, 64, 64, 128, 1, 2, 1>(p, s);
+    return dispatch_shape<RS_GDN, 64, 64, 128, 1, 2, 1>(p, s);
 }
 
 cudaError_t replay_launch(const ReplayParams &p, int kind, int P, int N, cudaStream_t s) {

@@ -47,8 +47,9 @@ struct PipeCfg {
     static constexpr int NP = N / SPLIT;                  // key rows per stage
     static constexpr int STAGE = NP * P * 4;              // bytes of one fp32 row block = one stage
     static_assert(NS >= SPLIT, "a folding head keeps all its row blocks resident");
-    // registers sized so that two CTAs fit on an SM (the draft-heavy T=8 shape excepted)
-    static constexpr int MIN_BLOCKS = TMAX <= 4 ? 2 : 1;
+    // registers sized so that two CTAs fit on an SM (two-stage rings; the
+    // draft-heavy T=8 shape excepted)
+    static constexpr int MIN_BLOCKS = (NS <= 2 && TMAX <= 4) ? 2 : 1;
 };
 
 // What one launch does to one sequence, from its pointers and the mode.
@@ -751,11 +752,16 @@ cudaError_t launch_pipe(const ReplayParams &p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-// Launch shapes.  Candidates are tried in order; the first whose heads per
-// unit divide the group and whose shared memory fits two CTAs on an SM wins,
-// else the first that fits one CTA.
+// Launch shapes, tried in order: two CTAs per SM with a two-stage ring (one
+// CTA's per-unit and per-head serial phases overlap the other's streaming);
+// else one CTA per SM with a deeper ring that covers those phases itself;
+// else one CTA with two stages.  Within a tier, the most heads per unit whose
+// count divides the group and whose shared memory fits.
 constexpr int kMaxSmemPerBlock = 227 * 1024;
 constexpr int kTwoPerSm = kMaxSmemPerBlock / 2 - 1024;
+#ifndef RS_DEEP_FIRST
+#define RS_DEEP_FIRST 0
+#endif
 
 template <class C>
 bool try_shape(const ReplayParams &p, int hpg, int limit, cudaStream_t s, cudaError_t &err) {
@@ -764,22 +770,26 @@ bool try_shape(const ReplayParams &p, int hpg, int limit, cudaStream_t s, cudaEr
     return true;
 }
 
-template <int KIND, int P, int N, int NC, int TMAX, int SPLIT, int NS, int... HUS>
+template <int KIND, int P, int N, int NC, int TMAX, int SPLIT, int... HUS>
 cudaError_t launch_shape(const ReplayParams &p, cudaStream_t s) {
     const int hpg = p.H / p.G;
     cudaError_t e = cudaErrorInvalidValue;
-    for (const int limit : {kTwoPerSm, kMaxSmemPerBlock})
-        if ((try_shape<PipeCfg<KIND, P, N, HUS, TMAX, NC, NS, SPLIT>>(p, hpg, limit, s, e) || ...)) return e;
+    constexpr int DEEP = 4;
+    if (!RS_DEEP_FIRST &&
+        (try_shape<PipeCfg<KIND, P, N, HUS, TMAX, NC, 2, SPLIT>>(p, hpg, kTwoPerSm, s, e) || ...))
+        return e;
+    if ((try_shape<PipeCfg<KIND, P, N, HUS, TMAX, NC, DEEP, SPLIT>>(p, hpg, kMaxSmemPerBlock, s, e) || ...)) return e;
+    if ((try_shape<PipeCfg<KIND, P, N, HUS, TMAX, NC, 2, SPLIT>>(p, hpg, kMaxSmemPerBlock, s, e) || ...)) return e;
     return cudaErrorInvalidConfiguration;
 }
 
 // Verify launches instantiate the draft-count buckets 1, 4 and 8.
-template <int KIND, int P, int N, int NC, int SPLIT, int NS, int... HUS>
+template <int KIND, int P, int N, int NC, int SPLIT, int... HUS>
 cudaError_t dispatch_shape(const ReplayParams &p, cudaStream_t s) {
     const int T = p.mode == MODE_VERIFY ? p.T : 1;
-    if (T <= 1) return launch_shape<KIND, P, N, NC, 1, SPLIT, NS, HUS...>(p, s);
-    if (T <= 4) return launch_shape<KIND, P, N, NC, 4, SPLIT, NS, HUS...>(p, s);
-    return launch_shape<KIND, P, N, NC, 8, SPLIT, NS, HUS...>(p, s);
+    if (T <= 1) return launch_shape<KIND, P, N, NC, 1, SPLIT, HUS...>(p, s);
+    if (T <= 4) return launch_shape<KIND, P, N, NC, 4, SPLIT, HUS...>(p, s);
+    return launch_shape<KIND, P, N, NC, 8, SPLIT, HUS...>(p, s);
 }
 
 // One translation unit per family / slab shape (compiled in parallel).
