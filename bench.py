@@ -78,7 +78,8 @@ def measured_peaks() -> dict:
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("rs_replay.cuh", "rs_replay.cu", "rs_replay_m2.cu", "rs_replay_gdn.cu", "rs_common.cuh"):
+    for name in ("rs_plan.cuh", "rs_replay_rows.cuh", "rs_replay_cols.cuh", "rs_replay.cu", "rs_replay_m2.cu",
+                 "rs_replay_gdn.cu", "rs_common.cuh"):
         with open(os.path.join(ROOT, "rs_decode_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -513,8 +514,8 @@ def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
 
     achieved = m["bytes_per_launch"] / (m["launch_ms"] * 1e-3) / 1e9
     clk = ClockSampler.summarise(m["clock_rows"], *m["t_wall"]) if m["clock_rows"] else None
-    kernel = {"mamba2": "replay_pipe_kernel<mamba2, P=64, N=128, HU=8, TMAX=1, NC=256, NS=2, SPLIT=1>",
-              "gdn": "replay_pipe_kernel<gdn, P=128, N=128, HU=2, TMAX=1, NC=256, NS=2, SPLIT=2>"}[w.kind]
+    kernel = {"mamba2": "rows::replay_pipe_kernel<mamba2, P=64, N=128, HU=8, TMAX=1, NC=256, NS=2, SPLIT=1>",
+              "gdn": "cols::replay_pipe_kernel<gdn, P=128, N=128, TMAX=1> (launch: HU=2, NS=4, 2 CTAs/SM)"}[w.kind]
     out = {
         "metric": METRIC,
         "value": w.B * K * world / (ms_total * 1e-3),

@@ -90,11 +90,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
         : "memory");
     return ok != 0;
 }
+// As mbar_try_wait, but a thread whose phase is not complete yet sleeps until
+// it completes or kSleepHintNs pass, instead of returning at once: waiting
+// warps then take no issue slots from the working ones.
+constexpr unsigned kSleepHintNs = 100000;  // 100 us
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSleepHintNs)
+        : "memory");
+    return ok != 0;
+}
 // Waits for the phase of the given parity to complete; false on time-out.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_sleep(bar, parity)) {
         if (global_ns() - t0 > kWaitLimitNs) return false;
     }
     return true;
@@ -111,6 +124,22 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, unsign
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
+
+// Tiled tensor copy (TMA) of one box global -> shared, completing on `bar`,
+// evict-first in L2.  `tmap` is the address of a CUtensorMap kernel parameter;
+// c0..c3 are the box's start coordinates, innermost first.
+__device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, int c0, int c1, int c2, int c3,
+                                            uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .b64 pol;\n\t"
+        "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], pol;\n\t}" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 
 // Named barrier over the first `count` threads of the CTA (the consumer
 // warps) that also ORs a flag over them: every participant gets the same

@@ -1,0 +1,1092 @@
+// Output-only replay kernels of the ReplaySSM decode path (Mamba-2 and Gated
+// DeltaNet): standard decode with the flush route fused, speculative verify
+// with the fold of committed records fused, forced flush, and materialise.
+//
+// The state of one (sequence, head) is S = gamma * S_c + sum_r w_r v_r k_r^T
+// over the records r since the checkpoint S_c ("ReplaySSM: Cache SSM Inputs,
+// Not State", section "How it works").  A step reads the checkpoint once and
+// writes only outputs and the appended record; the checkpoint is rewritten
+// only by a fold (the "flush route").
+//
+// Kernel structure: a persistent, warp-specialised pipeline with three roles.
+//   * Work unit = HU heads of one sequence that share one key group.
+//   * A producer warp (one elected lane) streams each unit's checkpoint slabs,
+//     once the prep warps have planned the unit, into a ring of NS shared-
+//     memory stages with tiled tensor copies (TMA) that complete on mbarriers.  A stage is one row block of a slab: 16 KiB of whole key rows
+//     (contiguous in HBM), stored with the 128-byte swizzle, so a slab takes
+//     P*sizeof(elem)/128 stages.
+//   * Three prep warps plan each unit from the sequence's pointers and build
+//     its context one unit ahead of the consumers, in a double buffer: they
+//     stage every small operand (buffered records, the step's keys / queries
+//     / values, per-head constants) with cp.async, append the new records, and
+//     compute the key.query dots, the decay coefficients (product scans over
+//     the records), the fp32 dot vectors and the record parts of the outputs.
+//   * Four consumer warps only stream the heads.  Per head each warp works
+//     alone on its own value columns: it dots them with the query (GDN: key
+//     and query) vectors over every row block, reduces over its lanes with
+//     shuffles, writes the outputs (GDN: runs the recurrence over the drafts
+//     that gives the correction u), and on a fold rewrites its columns as
+//     gamma S_c + (V diag(w)) K^T from the staged copy.  No barrier spans the
+//     consumer warps; a stage goes back to the producer once every consumer
+//     warp has read it, a context once every consumer warp is done with it.
+// Slabs are key-major ([N][P], value index contiguous).  A stage holds its rows
+// as 128-byte lines (row-major, NCB lines per row); 16-byte chunk c of line l
+// sits at l*128 + ((c ^ (l & 7)) << 4).  Each shared-memory phase of 8 lanes
+// reads chunks that land in 8 different bank groups (see WGeo).
+//
+// Per-sequence pointers (base, h, nd) are read once per unit by the prep warps;
+// the last unit to have read them (an arrival counter) writes the new values,
+// so no second launch is needed.  Every wait is bounded: on a time-out the CTA
+// raises RS_DEV_TIMEOUT, drains its copies and returns.
+#pragma once
+
+#include <cuda.h>
+#include <string.h>
+
+#include "rs_plan.cuh"
+
+namespace rs {
+namespace cols {
+
+// Compile-time shape of one kernel instantiation: family, slab shape and the
+// draft-count bucket.  Heads per unit (HU) and ring depth (NS) are launch
+// arguments.
+template <int KIND_, int P_, int N_, int TMAX_>
+struct RCfg {
+    static constexpr int KIND = KIND_, P = P_, N = N_, TMAX = TMAX_;
+    static constexpr int NCW = 4;                         // consumer warps (warps 0..NCW-1)
+    static constexpr int NPW = 3;                         // prep warps (after the producer warp)
+    static constexpr int NT = 32 * (NCW + 1 + NPW);       // + the producer warp (warp NCW)
+    static constexpr int PREP0 = 32 * (NCW + 1);          // first prep thread
+    static constexpr int NPT = 32 * NPW;                  // prep threads
+    // vectors dotted with every slab: Mamba-2 the queries C_i; GDN the keys
+    // k_{m_i} (slots 0..TMAX-1) and the queries q_i (slots TMAX..2TMAX-1)
+    static constexpr int JP = (KIND == RS_GDN ? 2 : 1) * TMAX;
+    static constexpr int STAGE = N * 128;                 // one row block: N lines of 128 bytes
+    static constexpr int QW = JP < 4 ? JP : 4;            // query floats per shared-memory vector
+    static constexpr int QC = JP / QW;                    // vectors per key row
+    static constexpr int MIN_BLOCKS = 2;                  // two CTAs per SM
+    // dot vectors per pass over a staged head: at most 64 partial sums per lane
+    template <int VEC> static constexpr int jn() { return VEC * JP <= 64 ? JP : 64 / VEC; }
+    static_assert(N % 8 == 0 && N <= 256, "a stage is one tensor box");
+};
+
+// Where a consumer warp's lanes sit in a stage of element type TE.  A row of
+// the slab is NCB 128-byte lines; warp w owns CPW 16-byte chunks of line
+// position cb = w / WPC; lane = cg + CPW * rg takes chunk cg in the rows
+// row(rg) + RGW * k of every row block.  One shared-memory phase of 8 lanes
+// reads CPW chunks in each of 8/CPW rows; row(rg) rotates the low bits of rg
+// by SH = log2(CPW / NCB) (0 or 1) so that those rows differ in the line bits
+// just above the chunk bits: the 8 chunks then fall in 8 different bank groups
+// under the swizzle.
+template <class C, typename TE>
+struct WGeo {
+    static constexpr int ESZ = sizeof(TE), VEC = 16 / ESZ;  // elements per 16-byte chunk
+    static constexpr int NCB = C::P * ESZ / 128;            // lines per row = row blocks (stages) per slab
+    static constexpr int WPC = C::NCW / NCB;                // warps per line position
+    static constexpr int CPW = 8 / WPC;                     // chunks per warp
+    static constexpr int LCG = ilog2(CPW);
+    static constexpr int RGW = 32 / CPW;                    // row groups per warp
+    static constexpr int LR = ilog2(RGW);
+    static constexpr int LPH = ilog2(8 / CPW);              // log2 rows per shared-memory phase
+    static constexpr int SH = ilog2(CPW / NCB);              // row rotation
+    static constexpr int RB = C::N / NCB;                   // rows per row block
+    static constexpr int RK = RB / RGW;                     // rows per lane per row block
+    static constexpr int LSTRIDE = RGW * NCB;               // lines between a lane's rows
+    static constexpr int CBE = 128 / ESZ;                   // elements per line
+    static constexpr int JN = C::template jn<VEC>();        // dot vectors per pass
+    static constexpr int NPASS = C::JP / JN;                // passes over the staged head
+    static constexpr int M = VEC * JN;                      // partial sums per lane and pass
+    static_assert(NCB >= 1 && C::NCW % NCB == 0 && CPW * WPC == 8 && CPW * C::NCW == 8 * NCB, "warp tiling");
+    static_assert(SH <= 1 && LSTRIDE % 8 == 0 && RGW >= (1 << (LPH + SH)), "a lane keeps one swizzle phase");
+    static_assert(RB * NCB * 128 == C::STAGE && RB % RGW == 0, "a row block is one stage");
+    // the row (within a row block) of row group rg
+    static __device__ __forceinline__ int row_of(int rg) {
+        if constexpr (SH == 0) {
+            return rg;
+        } else {
+            constexpr int MSK = (2 << LPH) - 1;
+            const int low = rg & MSK;
+            return (rg & ~MSK) | (((low << 1) | (low >> LPH)) & MSK);
+        }
+    }
+};
+
+// Header of a unit context: the plan and the unit's place.
+struct UnitHdr {
+    SeqPlan s;
+    int b, h0;
+};
+
+// Shared-memory carve-up, byte offsets from a 1024-byte aligned base (stages
+// first, so every stage is 1024-byte aligned as the swizzle requires).  The
+// unit context (ctx*, offsets within one context) is double-buffered; the
+// prep warps' scratch (d1, d2, sr, cst and the staged GDN u records xr) is not:
+// a fold gathers the value records it needs from global memory into the
+// consumer warps' scratch (fcf: fw_r v_r for the warp's P/NCW columns).
+struct RSmem {
+    int stages, bars, abort, d1, d2, sr, cst, xr, fcf, ctx0, ctx_bytes;
+    int hdr, kraw, ar, vb, bt, c1, c2, g1, g2, fw, gF, pre1, pre2, qs, unew;  // within a context
+    int total;
+};
+
+__host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
+
+template <class C>
+__host__ __device__ inline RSmem replay_smem(int cap, int HU, int NS) {
+    constexpr int TMAX = C::TMAX, P = C::P, N = C::N;
+    constexpr bool GDN = C::KIND == RS_GDN;
+    RSmem s;
+    int o = 0;
+    s.stages = o; o += NS * C::STAGE;
+    s.bars = o;   o += al16((2 * NS + 6) * 8);                      // stage and context barriers
+    s.abort = o;  o += 16;
+    s.d1 = o;     o += al16(cap * TMAX * 4);                        // k_r . q_i (GDN: k_r . k_{m_i})
+    s.d2 = o;     o += GDN ? al16(cap * TMAX * 4) : 0;              // GDN k_r . q_i
+    s.sr = o;     o += al16(HU * cap * 4);                          // Mamba-2 dt_r
+    s.cst = o;    o += al16(2 * HU * 4);                            // Mamba-2 A_h, D_h
+    s.xr = o;     o += GDN ? al16(HU * cap * P * 4) : 0;            // GDN committed u (fp32) per record
+    s.fcf = o;    o += al16(C::NCW * cap * (P / C::NCW) * 4);       // consumer warps' fold coefficients
+    int c = 0;
+    s.hdr = c;    c += al16((int)sizeof(UnitHdr));
+    s.kraw = c;   c += al16((cap + TMAX) * N * 2);                  // bf16 keys (rows < cap), queries (cap + i)
+    s.ar = c;     c += al16(HU * cap * 4);                          // decays alpha_r
+    s.vb = c;     c += GDN ? al16(TMAX * HU * P * 2) : 0;           // GDN drafts' v (bf16)
+    s.bt = c;     c += GDN ? al16(TMAX * HU * 4) : 0;               // GDN drafts' beta
+    s.c1 = c;     c += al16(HU * TMAX * cap * 4);
+    s.c2 = c;     c += GDN ? al16(HU * TMAX * cap * 4) : 0;
+    s.g1 = c;     c += al16(HU * TMAX * 4);
+    s.g2 = c;     c += al16(HU * TMAX * 4);
+    s.fw = c;     c += al16(HU * cap * 4);
+    s.gF = c;     c += al16(HU * 4);
+    s.pre1 = c;   c += al16(HU * TMAX * P * 4);                     // record parts of the outputs
+    s.pre2 = c;   c += GDN ? al16(HU * TMAX * P * 4) : 0;
+    s.qs = c;     c += al16(N * C::JP * 4);                         // fp32 dot vectors, [QC][N][QW]
+    s.unew = c;   c += GDN ? al16(HU * TMAX * P * 4) : 0;           // GDN: u of this launch's records
+    s.ctx_bytes = c;
+    s.ctx0 = o;   o += 2 * c;
+    s.total = o;
+    return s;
+}
+
+// VEC consecutive bf16 values (VEC = 4: 8-byte aligned, VEC = 8: 16-byte aligned) as fp32.
+template <int VEC>
+__device__ __forceinline__ void load_bf16_vec(const uint16_t *src, float (&out)[VEC]) {
+    if constexpr (VEC == 8) {
+        unpack<uint16_t, 8>(ld_u4(src), out);
+    } else {
+        static_assert(VEC == 4, "4 or 8 values");
+        const uint2 u = *reinterpret_cast<const uint2 *>(src);
+        out[0] = bf2f(u.x & 0xffffu); out[1] = __uint_as_float(u.x & 0xffff0000u);
+        out[2] = bf2f(u.y & 0xffffu); out[3] = __uint_as_float(u.y & 0xffff0000u);
+    }
+}
+
+// VEC consecutive fp32 values (16-byte aligned).
+template <int VEC>
+__device__ __forceinline__ void load_f32_vec(const float *src, float (&out)[VEC]) {
+#pragma unroll
+    for (int c = 0; c < VEC / 4; ++c) {
+        const float4 f = reinterpret_cast<const float4 *>(src)[c];
+        out[4 * c] = f.x; out[4 * c + 1] = f.y; out[4 * c + 2] = f.z; out[4 * c + 3] = f.w;
+    }
+}
+
+// Dot-vector slots J0 .. J0+JN-1 of key row n ([QC][N][QW] fp32 layout: the
+// lanes of a warp read consecutive rows, i.e. consecutive addresses).
+template <class C, int J0, int JN>
+__device__ __forceinline__ void load_q(const float *qs, int n, float (&qv)[JN]) {
+    constexpr int QW = C::QW, N = C::N;
+    static_assert(J0 % QW == 0 && JN % QW == 0, "whole vectors");
+#pragma unroll
+    for (int c = 0; c < JN / QW; ++c) {
+        const float *src = qs + ((size_t)(J0 / QW + c) * N + n) * QW;
+        if constexpr (QW == 4) {
+            const float4 f = *reinterpret_cast<const float4 *>(src);
+            qv[4 * c] = f.x; qv[4 * c + 1] = f.y; qv[4 * c + 2] = f.z; qv[4 * c + 3] = f.w;
+        } else if constexpr (QW == 2) {
+            const float2 f = *reinterpret_cast<const float2 *>(src);
+            qv[0] = f.x; qv[1] = f.y;
+        } else {
+            qv[0] = *src;
+        }
+    }
+}
+
+// Sum of v over the RGW row-group lanes of a warp (lane bits LCG and up), by
+// recursive halving while more than NV values remain per lane, then by
+// butterfly.  Afterwards a lane holds, in v[0..NV), the totals of entries
+// a0 .. a0+NV-1 with a0 = (rg >> (LR - H)) * NV, H = log2(M / NV) halvings.
+template <int M, int SZ, int NV, int MASK, int LCG>
+struct RowReduce {
+    static __device__ __forceinline__ void run(float (&v)[M], int rg) {
+        if constexpr (MASK >= 1) {
+            if constexpr (SZ > NV) {
+                constexpr int HALF = SZ / 2;
+                const bool up = (rg & MASK) != 0;
+#pragma unroll
+                for (int i = 0; i < HALF; ++i) {
+                    const float send = up ? v[i] : v[i + HALF];
+                    const float keep = up ? v[i + HALF] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, MASK << LCG);
+                }
+                RowReduce<M, HALF, NV, MASK / 2, LCG>::run(v, rg);
+            } else {
+#pragma unroll
+                for (int i = 0; i < NV; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], MASK << LCG);
+                RowReduce<M, SZ, NV, MASK / 2, LCG>::run(v, rg);
+            }
+        }
+    }
+};
+
+// The lane's VEC columns times dot-vector slots J0 .. J0+JN-1 over the lane's
+// RK rows of one staged row block (rows row0, row0 + RGW, ... of the slab),
+// added to acc[e * JN + jj].
+template <class C, typename TE, int J0>
+__device__ __forceinline__ void dot_rows(const uint8_t *lane_base, const float *qs, int row0,
+                                         float (&acc)[WGeo<C, TE>::M]) {
+    using W = WGeo<C, TE>;
+    constexpr int VEC = W::VEC, RGW = W::RGW, JN = W::JN;
+#pragma unroll
+    for (int k = 0; k < W::RK; ++k) {
+        float sv[VEC], qv[JN];
+        unpack<TE, VEC>(ld_u4(lane_base + (size_t)k * RGW * W::NCB * 128), sv);
+        load_q<C, J0, JN>(qs, row0 + k * RGW, qv);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+#pragma unroll
+            for (int jj = 0; jj < JN; ++jj) acc[e * JN + jj] = fmaf(sv[e], qv[jj], acc[e * JN + jj]);
+    }
+}
+
+// Sums over the warp's row groups, keeping at least KEEP entries per lane.
+template <class C, typename TE, int KEEP>
+__device__ __forceinline__ void reduce_rows(float (&acc)[WGeo<C, TE>::M], int rg) {
+    using W = WGeo<C, TE>;
+    constexpr int NV = W::M / W::RGW > KEEP ? W::M / W::RGW : KEEP;
+    RowReduce<W::M, W::M, NV, W::RGW / 2, W::LCG>::run(acc, rg);
+}
+
+// ---------------------------------------------------------------------------
+// Producer: stream each unit's row blocks once the prep warps have planned it.
+template <class C>
+__device__ __forceinline__ void producer(const ReplayParams &p, uint8_t *sm, const RSmem &L, int units, int HU,
+                                         int NS, const CUtensorMap *map_hp, const CUtensorMap *map_lp) {
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + L.bars), *empty = full + NS, *cplan = empty + NS;
+    uint64_t *cempty = cplan + 4;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
+    int st = 0, ph = 0, issued = 0, cu = 0;
+    bool stop = false;
+    for (int u = blockIdx.x; u < units && !stop; u += gridDim.x, ++cu) {
+        const int buf = cu & 1;
+        if (!wait_or_abort(cplan + buf, (cu >> 1) & 1, abort_flag, p.status)) break;
+        const UnitHdr hd = *reinterpret_cast<const UnitHdr *>(sm + L.ctx0 + buf * L.ctx_bytes + L.hdr);
+        // the prep warps rebuild this context only after this arrival (and the
+        // consumer warps'), so no plan phase can pass unread
+        mbar_arrive(cempty + buf);
+        if (!hd.s.work) continue;
+        const bool lp = plan_reads_lp(p, hd.s);
+        const CUtensorMap *map = lp ? map_lp : map_hp;
+        const int ncb = C::P * (lp ? 2 : 4) / 128, rb_rows = C::N / ncb;
+        for (int j = 0; j < HU && !stop; ++j) {
+            for (int rb = 0; rb < ncb; ++rb) {
+                if (!wait_or_abort(empty + st, ph ^ 1, abort_flag, p.status)) { stop = true; break; }
+                mbar_arrive_expect_tx(full + st, C::STAGE);
+                tma_load_4d(sm + L.stages + (size_t)st * C::STAGE, map, 0, 0, rb * rb_rows, hd.b * p.H + hd.h0 + j,
+                            full + st);
+                ++issued;
+                if (++st == NS) { st = 0; ph ^= 1; }
+            }
+        }
+    }
+    if (*abort_flag) {
+        // drain: wait (bounded) for the copies this thread may still have in flight,
+        // the last min(NS, issued) ones, walking the ring backwards
+        int s = st, q = ph;
+        for (int k = 0; k < NS && k < issued; ++k) {
+            if (--s < 0) { s = NS - 1; q ^= 1; }
+            mbar_wait(full + s, q);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Where the fold of one head finds the value vector of record r: the
+// committed records (r < hc) in the record buffer, this launch's records in
+// the step inputs (Mamba-2 x) or in the context (GDN u).
+struct FoldSrc {
+    const uint8_t *committed;  // record buffer, slot 0 of this (sequence, head)
+    const uint8_t *fresh;      // record hc of this (sequence, head)
+    size_t slot_stride, fresh_stride;  // bytes between slots / between this launch's records
+    int base, hc, cap;
+};
+
+// Gathers fw_r v_r[p] for r < F and the warp's WC = P/NCW value columns
+// (from column wcol0 on) into the warp's scratch cfs[r][WC], fp32.  All the
+// loads of a head are independent and issued together.
+template <class C>
+__device__ __forceinline__ void gather_fold_coefs(float *cfs, const FoldSrc &fs, const float *fw, int F, int j,
+                                                  int wcol0, int lane) {
+    constexpr int WC = C::P / C::NCW, Q = WC / 4;  // four columns per item
+    constexpr int VSZ = C::KIND == RS_MAMBA2 ? 2 : 4;
+    for (int i = lane; i < F * Q; i += 32) {
+        const int r = i / Q, c4 = i % Q;
+        int sl = fs.base + r;
+        if (sl >= fs.cap) sl -= fs.cap;
+        const uint8_t *src = (r < fs.hc ? fs.committed + (size_t)sl * fs.slot_stride
+                                        : fs.fresh + (size_t)(r - fs.hc) * fs.fresh_stride) +
+                             (size_t)(wcol0 + 4 * c4) * VSZ;
+        float v[4];
+        if constexpr (C::KIND == RS_MAMBA2) load_bf16_vec<4>(reinterpret_cast<const uint16_t *>(src), v);
+        else load_f32_vec<4>(reinterpret_cast<const float *>(src), v);
+        const float w = fw[j * fs.cap + r];
+        *reinterpret_cast<float4 *>(cfs + r * WC + 4 * c4) = make_float4(w * v[0], w * v[1], w * v[2], w * v[3]);
+    }
+    __syncwarp();
+}
+
+// Fold of the lane's columns of one staged row block:
+//   S_new = gF S_c + sum_{r<F} (fw_r v_r) k_r^T
+// written to the checkpoint (both copies as present) or to the materialise
+// output.  The coefficients fw_r v_r come from the warp's scratch (lane
+// columns from lcol on); each is applied to the lane's RK rows (row0, row0 +
+// RGW, ...).
+template <class C, typename TE>
+__device__ __forceinline__ void fold_block(const ReplayParams &p, const uint8_t *lane_base, const uint16_t *kraw,
+                                           const float *cfs, int lcol, float gf, int F, int row0, int col0,
+                                           size_t goff, bool materialize) {
+    using W = WGeo<C, TE>;
+    constexpr int VEC = W::VEC, RK = W::RK, RGW = W::RGW, N = C::N, P = C::P, WC = C::P / C::NCW;
+    float o[RK][VEC];
+#pragma unroll
+    for (int k = 0; k < RK; ++k) {
+        unpack<TE, VEC>(ld_u4(lane_base + (size_t)k * RGW * W::NCB * 128), o[k]);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) o[k][e] *= gf;
+    }
+    for (int r = 0; r < F; ++r) {
+        float cf[VEC];
+        load_f32_vec<VEC>(cfs + r * WC + lcol, cf);
+        const uint16_t *kr = kraw + (size_t)r * N + row0;
+#pragma unroll
+        for (int k = 0; k < RK; ++k) {
+            const float kv = bf2f(kr[k * RGW]);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) o[k][e] = fmaf(cf[e], kv, o[k][e]);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < RK; ++k) {
+        const size_t off = goff + (size_t)(row0 + k * RGW) * P + col0;
+        if (materialize) {
+            store_f32<VEC>(p.out + off, o[k]);
+        } else {
+            if (p.ckpt_hp) store_f32<VEC>(p.ckpt_hp + off, o[k]);
+            if (p.ckpt_lp) store_bf16<VEC>(p.ckpt_lp + off, o[k]);
+        }
+    }
+}
+
+// Ring position q of the stage ring: every consumer warp waits for every stage
+// in ring order and arrives once on each, after its last read; the producer
+// refills a stage only when all have.  A parity wait cannot tell a phase from
+// the one two phases later, so no warp may skip a stage or fall a ring behind.
+__device__ __forceinline__ bool wait_stage(uint64_t *full, int q, int NS, volatile int *abort_flag, uint32_t *status,
+                                           bool ok) {
+    ok = ok && wait_or_abort(full + q % NS, (unsigned)(q / NS) & 1u, abort_flag, status);
+    return __all_sync(0xffffffffu, ok);
+}
+__device__ __forceinline__ void release_stage(uint64_t *empty, int q, int NS) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(empty + q % NS);
+}
+
+// One pass of a warp over a head's row blocks (ring positions q0 ..
+// q0+NCB-1) for dot-vector slots J0 .. J0+JN-1.  A streamed head waits for,
+// reads and hands back each block in turn; a held head's blocks are already
+// resident and stay so.  Returns false on abort.
+template <class C, typename TE, int J0>
+__device__ __forceinline__ bool head_pass(float (&acc)[WGeo<C, TE>::M], const ReplayParams &p, const uint8_t *stages,
+                                          int lane_off, int q0, int NS, uint64_t *full, uint64_t *empty,
+                                          volatile int *abort_flag, const float *qs, int rg, bool hold) {
+    using W = WGeo<C, TE>;
+    bool ok = true;
+#pragma unroll
+    for (int a = 0; a < W::M; ++a) acc[a] = 0.f;
+#pragma unroll 1
+    for (int rb = 0; rb < W::NCB; ++rb) {
+        const int q = q0 + rb;
+        if (!hold && !(ok = wait_stage(full, q, NS, abort_flag, p.status, ok))) break;
+        dot_rows<C, TE, J0>(stages + (size_t)(q % NS) * C::STAGE + lane_off, qs, rb * W::RB + rg, acc);
+        if (!hold) release_stage(empty, q, NS);
+    }
+    return ok;
+}
+
+// ---------------------------------------------------------------------------
+// Prep warps: build the context of one unit (everything but the slab stream)
+// in the context buffer `cx`.  Returns false when the CTA aborts.
+template <class C>
+__device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, const RSmem &L, uint8_t *cx,
+                                          const SeqPlan &s, const int b, const int h0, const int HU) {
+    constexpr int KIND = C::KIND, P = C::P, N = C::N, TMAX = C::TMAX, NPT = C::NPT, JP = C::JP;
+    const int tp = threadIdx.x - C::PREP0, lane = tp & 31, pw = tp >> 5;
+    const int H = p.H, G = p.G, cap = p.cap;
+    const int g = h0 / (H / G);
+    const int base = s.base, hc = s.hc, T = s.T, F = s.F;
+    const bool append = s.append;
+    const int nrec = hc + T;
+    auto slot = [&](int r) { return (base + r) % cap; };
+
+    float *d1 = reinterpret_cast<float *>(sm + L.d1), *d2 = reinterpret_cast<float *>(sm + L.d2);
+    float *sr = reinterpret_cast<float *>(sm + L.sr);
+    float *cst = reinterpret_cast<float *>(sm + L.cst);      // A_h (HU), D_h (HU)
+    uint16_t *kraw = reinterpret_cast<uint16_t *>(cx + L.kraw);
+    float *uf = reinterpret_cast<float *>(sm + L.xr);        // GDN committed u (fp32)
+    float *ar = reinterpret_cast<float *>(cx + L.ar);
+    uint16_t *vb = reinterpret_cast<uint16_t *>(cx + L.vb);
+    float *bt = reinterpret_cast<float *>(cx + L.bt);
+    float *c1 = reinterpret_cast<float *>(cx + L.c1), *c2 = reinterpret_cast<float *>(cx + L.c2);
+    float *g1 = reinterpret_cast<float *>(cx + L.g1), *g2 = reinterpret_cast<float *>(cx + L.g2);
+    float *fw = reinterpret_cast<float *>(cx + L.fw), *gF = reinterpret_cast<float *>(cx + L.gF);
+    float *pre1 = reinterpret_cast<float *>(cx + L.pre1), *pre2 = reinterpret_cast<float *>(cx + L.pre2);
+    float *qs = reinterpret_cast<float *>(cx + L.qs);
+
+    // Mamba-2 step-5 task of this thread (one head, 8 value columns): the first
+    // 8 records' x are loaded now, so that their latency overlaps the staging
+    constexpr int PC8 = P / 8;
+    const int x_hd = tp / PC8, x_pc = tp % PC8;
+    const bool x_task = KIND == RS_MAMBA2 && T > 0 && x_hd < HU;
+    const uint16_t *xbuf = static_cast<const uint16_t *>(p.buf_v);
+    auto x_src = [&](int r) {
+        return (r < hc ? xbuf + (((size_t)b * cap + slot(r)) * H + h0 + x_hd) * P
+                       : p.x + (((size_t)b * T + (r - hc)) * H + h0 + x_hd) * P) + 8 * x_pc;
+    };
+    uint4 xv[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) xv[t] = x_task && t < nrec ? ld_u4(x_src(t)) : make_uint4(0u, 0u, 0u, 0u);
+
+    // ---- 1. one batch of cp.async copies for every small operand of the unit
+    {
+        constexpr int KC = N / 8;  // 16-byte chunks per key row
+        for (int i2 = tp; i2 < (nrec + T) * KC; i2 += NPT) {
+            const int rr = i2 / KC, c = i2 % KC;
+            const uint16_t *src;
+            if (rr < hc) src = p.buf_k + (((size_t)b * cap + slot(rr)) * G + g) * N;
+            else if (rr < nrec) src = (KIND == RS_MAMBA2 ? p.Bm : p.k) + (((size_t)b * T + (rr - hc)) * G + g) * N;
+            else src = (KIND == RS_MAMBA2 ? p.Cm : p.q) + (((size_t)b * T + (rr - nrec)) * G + g) * N;
+            const int row = rr < nrec ? rr : cap + (rr - nrec);
+            cp_async16(kraw + (size_t)row * N + 8 * c, src + 8 * c);
+        }
+        if (KIND == RS_MAMBA2) {
+            // (the records' x are read straight from global memory where needed)
+            // A (forms the new records' decays) and D (the skip term of the
+            // outputs) only exist for launches that append records; flush and
+            // materialise pass neither
+            for (int i2 = tp; i2 < (T > 0 ? HU : 0); i2 += NPT) {
+                cp_async4(cst + i2, p.A + h0 + i2);
+                if (p.D) cp_async4(cst + HU + i2, p.D + h0 + i2);
+                else cst[HU + i2] = 0.f;
+            }
+        } else {  // committed u (fp32); the drafts' v (bf16) and beta
+            constexpr int UC = P / 4, VC = P / 8;
+            for (int i2 = tp; i2 < HU * hc * UC; i2 += NPT) {
+                const int c = i2 % UC, r = (i2 / UC) % hc, hd = i2 / (UC * hc), hh = h0 + hd;
+                const float *src = static_cast<const float *>(p.buf_v) + (((size_t)b * cap + slot(r)) * H + hh) * P;
+                cp_async16(uf + ((size_t)hd * cap + r) * P + 4 * c, src + 4 * c);
+            }
+            for (int i2 = tp; i2 < T * HU * VC; i2 += NPT) {
+                const int c = i2 % VC, hd = (i2 / VC) % HU, i = i2 / (VC * HU);
+                cp_async16(vb + ((size_t)i * HU + hd) * P + 8 * c, p.v + (((size_t)b * T + i) * H + h0 + hd) * P + 8 * c);
+            }
+            for (int i2 = tp; i2 < T * HU; i2 += NPT) {
+                const int hd = i2 % HU, i = i2 / HU;
+                cp_async4(bt + i2, p.beta + ((size_t)b * T + i) * H + h0 + hd);
+            }
+        }
+        for (int i2 = tp; i2 < HU * nrec; i2 += NPT) {  // decays and value scales
+            const int r = i2 % nrec, hd = i2 / nrec, hh = h0 + hd;
+            if (r < hc) {
+                const size_t rec = ((size_t)b * cap + slot(r)) * H + hh;
+                cp_async4(ar + hd * cap + r, p.buf_a + rec);
+                if (KIND == RS_MAMBA2) cp_async4(sr + hd * cap + r, p.buf_s + rec);
+            } else {
+                const size_t bti = ((size_t)b * T + (r - hc)) * H + hh;
+                if (KIND == RS_MAMBA2) cp_async4(sr + hd * cap + r, p.dt + bti);
+                else cp_async4(ar + hd * cap + r, p.alpha + bti);
+            }
+        }
+        cp_async_wait_all();
+    }
+    if (named_sync_or(1, NPT, false)) return false;
+
+    // ---- 2. new records' decays; appends; the fp32 dot vectors
+    for (int i2 = tp; i2 < HU * T; i2 += NPT) {
+        const int i = i2 / HU, hd = i2 % HU, hh = h0 + hd, r = hc + i;
+        float a;
+        if (KIND == RS_MAMBA2) {  // alpha = exp(dt A), formed once when the record is appended
+            a = expf(sr[hd * cap + r] * cst[hd]);
+            ar[hd * cap + r] = a;
+        } else {
+            a = ar[hd * cap + r];
+        }
+        if (append) {
+            const size_t rec = ((size_t)b * cap + slot(r)) * H + hh;
+            p.buf_a[rec] = a;
+            if (KIND == RS_MAMBA2) p.buf_s[rec] = sr[hd * cap + r];
+        }
+    }
+    if (append) {
+        if ((h0 % (H / G)) == 0) {  // the group's first unit appends the keys
+            for (int i2 = tp; i2 < T * (N / 8); i2 += NPT) {
+                const int i = i2 / (N / 8), c = i2 % (N / 8);
+                uint16_t *dst = p.buf_k + (((size_t)b * cap + slot(hc + i)) * G + g) * N;
+                reinterpret_cast<uint4 *>(dst)[c] = reinterpret_cast<const uint4 *>(kraw + (size_t)(hc + i) * N)[c];
+            }
+        }
+        // (Mamba-2: the new records' x are appended by the step-5 tasks)
+    }
+    if (T > 0) {
+        // slot jj of row n: Mamba-2 C_jj; GDN k_{hc+jj} (jj < TMAX) or q_{jj-TMAX};
+        // slots past the launch's drafts are zero
+        for (int i2 = tp; i2 < N * JP; i2 += NPT) {
+            const int n = i2 % N, jj = i2 / N;
+            int row = -1;
+            if (KIND == RS_MAMBA2) {
+                if (jj < T) row = cap + jj;
+            } else if (jj < TMAX) {
+                if (jj < T) row = hc + jj;
+            } else if (jj - TMAX < T) {
+                row = cap + jj - TMAX;
+            }
+            qs[((size_t)(jj / C::QW) * N + n) * C::QW + jj % C::QW] = row >= 0 ? bf2f(kraw[(size_t)row * N + n]) : 0.f;
+        }
+    }
+
+    // ---- 3. key/query dot products of the group (8 lanes per dot)
+    if (T > 0) {
+        const int per = nrec * T;
+        const int ndots = (KIND == RS_GDN ? 2 : 1) * per;
+        for (int bd = 0; bd < ndots; bd += NPT / 8) {
+            const int d = bd + tp / 8, sub = tp % 8;
+            float acc = 0.f;
+            int r = 0, i = 0, which = 0;
+            if (d < ndots) {
+                which = d / per;
+                r = (d % per) / T;
+                i = d % T;
+                const uint16_t *a = kraw + (size_t)r * N;
+                // Mamba-2: k_r . q_i ; GDN which 0: k_r . k_{hc+i}, which 1: k_r . q_i
+                const uint16_t *bv = (KIND == RS_GDN && which == 0) ? kraw + (size_t)(hc + i) * N
+                                                                    : kraw + (size_t)(cap + i) * N;
+                for (int n = sub * 8; n < N; n += 64) {
+                    float fa[8], fb[8];
+                    unpack<uint16_t, 8>(ld_u4(a + n), fa);
+                    unpack<uint16_t, 8>(ld_u4(bv + n), fb);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc = fmaf(fa[e], fb[e], acc);
+                }
+            }
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+            if (d < ndots && sub == 0) (which == 0 ? d1 : d2)[r * TMAX + i] = acc;
+        }
+    }
+    if (named_sync_or(1, NPT, false)) return false;
+
+    // ---- 4. decay coefficients per head
+    // Record positions are 0-based; draft i sits at m_i = hc + i.  With
+    // E(r, m) = prod_{s=r+1..m} alpha_s and gamma(m) = prod_{s<=m} alpha_s:
+    //   Mamba-2  c1[i][r] = E(r, m_i) dt_r (k_r . q_i)   multiplies x_r[p] in y_i;  g1[i] = gamma(m_i)
+    //   GDN      c1[i][r] = E(r, m_i - 1) (k_r . k_{m_i})  (r < m_i)  -> S_{m_i - 1} k_{m_i}
+    //            c2[i][r] = E(r, m_i) (k_r . q_i)          (r <= m_i) -> S_{m_i} q_i
+    //            g1[i] = gamma(m_i - 1), g2[i] = gamma(m_i)
+    //   fold of F records: fw[r] = E(r, F-1) (times dt_r for Mamba-2), gF = gamma(F-1)
+    // One warp per head, one lane per record: a reverse product scan of
+    // v_s = (s < hc ? alpha_s : 1) gives E(r, hc-1) in lane r and gamma(hc-1)
+    // in lane 0; each further bound m (up to hc+T-1; F-1 is among them) takes
+    // one more factor: E(r, m) = E(r, m-1) alpha_m for r < m, E(m, m) = 1.
+    for (int hd = pw; hd < HU; hd += C::NPW) {
+        const float al = lane < nrec ? ar[hd * cap + lane] : 1.f;
+        const float dtr = KIND == RS_MAMBA2 && lane < nrec ? sr[hd * cap + lane] : 1.f;
+        float inc = lane < hc ? al : 1.f;  // inclusive: prod_{s >= lane} v_s
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float o = __shfl_down_sync(0xffffffffu, inc, off);
+            if (lane + off < 32) inc *= o;
+        }
+        float E = __shfl_down_sync(0xffffffffu, inc, 1);  // prod_{s > lane} v_s = E(lane, hc-1)
+        if (lane == 31) E = 1.f;
+        float gam = __shfl_sync(0xffffffffu, inc, 0);  // gamma(hc-1)
+        for (int m = hc - 1; m < hc + T; ++m) {
+            if (m >= hc) {
+                const float am = __shfl_sync(0xffffffffu, al, m);  // alpha_m (m < nrec <= 32)
+                E = lane < m ? E * am : 1.f;
+                gam *= am;
+            }
+            const int i = m - hc;  // the draft whose own position is m (-1: none)
+            if (lane < nrec) {
+                if (KIND == RS_MAMBA2) {
+                    if (i >= 0) c1[(hd * TMAX + i) * cap + lane] = lane <= m ? E * dtr * d1[lane * TMAX + i] : 0.f;
+                } else {
+                    if (i >= 0) c2[(hd * TMAX + i) * cap + lane] = lane <= m ? E * d2[lane * TMAX + i] : 0.f;
+                    if (i + 1 < T) c1[(hd * TMAX + i + 1) * cap + lane] = lane <= m ? E * d1[lane * TMAX + i + 1] : 0.f;
+                }
+                if (m == F - 1 && lane < F) fw[hd * cap + lane] = KIND == RS_MAMBA2 ? E * dtr : E;
+            }
+            if (lane == 0) {
+                if (i >= 0) {
+                    if (KIND == RS_MAMBA2) g1[hd * TMAX + i] = gam;
+                    else g2[hd * TMAX + i] = gam;
+                }
+                if (KIND == RS_GDN && i + 1 < T) g1[hd * TMAX + i + 1] = gam;
+                if (m == F - 1) gF[hd] = gam;
+            }
+        }
+        if (F == 0 && lane == 0) gF[hd] = 1.f;
+    }
+    if (named_sync_or(1, NPT, false)) return false;
+
+    // ---- 5. the parts of the outputs that come from the records, per value column
+    if (KIND == RS_MAMBA2 && T > 0) {
+        // rec_i[p] = sum_{r <= m_i} c1[i][r] x_r[p] + D x_{m_i}[p]: one task per
+        // head and 8 columns, all drafts at once; the records' x come from
+        // global memory, 8 records' loads in flight at a time (the first 8
+        // were issued before the staging).  The task also appends the new x.
+        if (x_task) {
+            const int hd = x_hd, pc = x_pc;
+            const float d = cst[HU + hd];
+            float a[TMAX][8];
+#pragma unroll
+            for (int i = 0; i < TMAX; ++i)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) a[i][e] = 0.f;
+            for (int r0 = 0; r0 < nrec; r0 += 8) {
+                if (r0 > 0) {
+#pragma unroll
+                    for (int t = 0; t < 8; ++t)
+                        xv[t] = r0 + t < nrec ? ld_u4(x_src(r0 + t)) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const int r = r0 + t;
+                    if (r >= nrec) break;
+                    if (append && r >= hc)
+                        *reinterpret_cast<uint4 *>(const_cast<uint16_t *>(xbuf) +
+                                                   (((size_t)b * cap + slot(r)) * H + h0 + hd) * P + 8 * pc) = xv[t];
+                    float xf[8];
+                    unpack<uint16_t, 8>(xv[t], xf);
+#pragma unroll
+                    for (int i = 0; i < TMAX; ++i) {
+                        if (i < T && r <= hc + i) {
+                            const float c = c1[(hd * TMAX + i) * cap + r] + (r == hc + i ? d : 0.f);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) a[i][e] = fmaf(c, xf[e], a[i][e]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < TMAX; ++i) {
+                if (i < T) {
+                    float4 *dst = reinterpret_cast<float4 *>(pre1 + (hd * TMAX + i) * P + 8 * pc);
+                    dst[0] = make_float4(a[i][0], a[i][1], a[i][2], a[i][3]);
+                    dst[1] = make_float4(a[i][4], a[i][5], a[i][6], a[i][7]);
+                }
+            }
+        }
+        if (named_sync_or(1, NPT, false)) return false;
+    }
+    // GDN: committed-record parts of S_{m_i-1} k_{m_i} and S_{m_i} q_i, four
+    // columns per task
+    if (KIND == RS_GDN && T > 0) {
+        constexpr int PC = P / 4;
+        for (int i2 = tp; i2 < HU * T * PC; i2 += NPT) {
+            const int pc = i2 % PC, i = (i2 / PC) % T, hd = i2 / (PC * T);
+            float s1[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+            const float *cc1 = c1 + (hd * TMAX + i) * cap, *cc2 = c2 + (hd * TMAX + i) * cap;
+#pragma unroll 4
+            for (int r = 0; r < hc; ++r) {
+                const float4 u = *reinterpret_cast<const float4 *>(uf + ((size_t)hd * cap + r) * P + 4 * pc);
+                const float a1 = cc1[r], a2 = cc2[r];
+                s1[0] = fmaf(a1, u.x, s1[0]); s1[1] = fmaf(a1, u.y, s1[1]);
+                s1[2] = fmaf(a1, u.z, s1[2]); s1[3] = fmaf(a1, u.w, s1[3]);
+                s2[0] = fmaf(a2, u.x, s2[0]); s2[1] = fmaf(a2, u.y, s2[1]);
+                s2[2] = fmaf(a2, u.z, s2[2]); s2[3] = fmaf(a2, u.w, s2[3]);
+            }
+            *reinterpret_cast<float4 *>(pre1 + (hd * TMAX + i) * P + 4 * pc) = make_float4(s1[0], s1[1], s1[2], s1[3]);
+            *reinterpret_cast<float4 *>(pre2 + (hd * TMAX + i) * P + 4 * pc) = make_float4(s2[0], s2[1], s2[2], s2[3]);
+        }
+        if (named_sync_or(1, NPT, false)) return false;
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// Consumer warps: the heads of one unit from its context `cx`, each warp on
+// its own value columns.  `it` is the ring position of the unit's first
+// stage.  Returns false when the CTA aborts.
+template <class C, typename TE>
+__device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm, const RSmem &L, const uint8_t *cx,
+                                              const SeqPlan &s, const int b, const int h0, const int HU,
+                                              const int NS, int &it) {
+    constexpr int KIND = C::KIND, P = C::P, N = C::N, TMAX = C::TMAX, JP = C::JP;
+    using W = WGeo<C, TE>;
+    constexpr int VEC = W::VEC, RGW = W::RGW, LR = W::LR, M = W::M, NCB = W::NCB, JN = W::JN, NPASS = W::NPASS;
+    constexpr int RB = W::RB;
+    static_assert(NPASS == 1 || NPASS == 2 || (NPASS == 4 && KIND == RS_GDN), "passes");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int H = p.H, cap = p.cap, mode = p.mode;
+    const int base = s.base, hc = s.hc, T = s.T, F = s.F;
+    const bool append = s.append, materialize = mode == MODE_MATERIALIZE;
+    const bool keep = s.fold || materialize;  // the staged head is read again by the fold
+    auto slot = [&](int r) { return (base + r) % cap; };
+
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + L.bars), *empty = full + NS;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
+    const uint16_t *kraw = reinterpret_cast<const uint16_t *>(cx + L.kraw);
+    float *unew = const_cast<float *>(reinterpret_cast<const float *>(cx + L.unew));  // GDN: u of new records
+    const float *ar = reinterpret_cast<const float *>(cx + L.ar);
+    const uint16_t *vb = reinterpret_cast<const uint16_t *>(cx + L.vb);
+    const float *bt = reinterpret_cast<const float *>(cx + L.bt);
+    const float *c1 = reinterpret_cast<const float *>(cx + L.c1), *c2 = reinterpret_cast<const float *>(cx + L.c2);
+    const float *g1 = reinterpret_cast<const float *>(cx + L.g1), *g2 = reinterpret_cast<const float *>(cx + L.g2);
+    const float *fw = reinterpret_cast<const float *>(cx + L.fw), *gF = reinterpret_cast<const float *>(cx + L.gF);
+    const float *pre1 = reinterpret_cast<const float *>(cx + L.pre1);
+    const float *pre2 = reinterpret_cast<const float *>(cx + L.pre2);
+    const float *qs = reinterpret_cast<const float *>(cx + L.qs);
+
+    const int cb = warp / W::WPC;                                  // the warp's line position in a row
+    const int cg = lane & (W::CPW - 1), rg = lane >> W::LCG;      // chunk among the warp's, row group
+    const int ch = (warp % W::WPC) * W::CPW + cg;                  // 16-byte chunk within the line
+    const int col0 = cb * W::CBE + ch * VEC;                       // first value column of the lane
+    const int row0 = W::row_of(rg);                                // the lane's first row in a row block
+    const int line0 = row0 * NCB + cb;
+    // later rows of the lane are LSTRIDE (a multiple of 8) lines further on: same swizzle
+    const int lane_off = line0 * 128 + ((ch ^ (line0 & 7)) << 4);
+    // the warp's value columns are contiguous: P / NCW of them from wcol0
+    const int wcol0 = cb * W::CBE + (warp % W::WPC) * W::CPW * VEC, lcol = col0 - wcol0;
+    float *cfs = reinterpret_cast<float *>(sm + L.fcf) + (size_t)warp * cap * (P / C::NCW);
+    // A head stays resident (all its row blocks) when the slab is read again
+    // after the reduction: by further passes, or by the fold (which for GDN
+    // takes in the u this launch computes).  Otherwise each row block is
+    // handed back as soon as every consumer warp has read it.
+    const bool hold = NPASS > 1 || keep;
+    const uint8_t *stages = sm + L.stages;
+    bool ok = true;
+    constexpr int VSZ = KIND == RS_MAMBA2 ? 2 : 4;
+    for (int j = 0; j < HU && ok; ++j) {
+        const int hh = h0 + j, q0 = it + j * NCB;
+        const size_t goff = ((size_t)b * H + hh) * ((size_t)N * P);
+        FoldSrc fs;
+        fs.committed = static_cast<const uint8_t *>(p.buf_v) + ((size_t)b * cap * H + hh) * P * VSZ;
+        fs.slot_stride = (size_t)H * P * VSZ;
+        if (KIND == RS_MAMBA2) {
+            fs.fresh = reinterpret_cast<const uint8_t *>(p.x) + ((size_t)b * T * H + hh) * P * 2;
+            fs.fresh_stride = (size_t)H * P * 2;
+        } else {
+            fs.fresh = reinterpret_cast<const uint8_t *>(unew + (size_t)j * TMAX * P);
+            fs.fresh_stride = (size_t)P * 4;
+        }
+        fs.base = base; fs.hc = hc; fs.cap = cap;
+        if (T == 0) {  // flush / materialise: fold only
+            gather_fold_coefs<C>(cfs, fs, fw, F, j, wcol0, lane);
+#pragma unroll 1
+            for (int rb = 0; rb < NCB; ++rb) {
+                const int q = q0 + rb;
+                if (!(ok = wait_stage(full, q, NS, abort_flag, p.status, ok))) break;
+                fold_block<C, TE>(p, stages + (size_t)(q % NS) * C::STAGE + lane_off, kraw, cfs, lcol, gF[j], F,
+                                  rb * RB + row0, col0, goff, materialize);
+                release_stage(empty, q, NS);
+            }
+            continue;
+        }
+        if (hold)
+            for (int rb = 0; rb < NCB && ok; ++rb) ok = wait_stage(full, q0 + rb, NS, abort_flag, p.status, ok);
+        if (!ok) break;
+        float acc[M];
+        if constexpr (KIND == RS_MAMBA2) {
+            // y_i[p] = gamma(m_i) (S_c q_i)[p] + rec_i[p]
+            constexpr int NV = M / RGW > 1 ? M / RGW : 1;
+            constexpr int HV = ilog2(M / NV);
+            const int a0 = (rg >> (LR - HV)) * NV;
+            const bool lead = (rg & ((1 << (LR - HV)) - 1)) == 0;
+            auto outputs = [&](int j0) {
+#pragma unroll
+                for (int t = 0; t < NV; ++t) {
+                    const int a = a0 + t, e = a / JN, i = j0 + a % JN;
+                    if (lead && i < T) {
+                        const int pp = col0 + e;
+                        p.y[(((size_t)b * T + i) * H + hh) * P + pp] =
+                            fmaf(g1[j * TMAX + i], acc[t], pre1[(j * TMAX + i) * P + pp]);
+                    }
+                }
+            };
+            ok = head_pass<C, TE, 0>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qs, row0, hold);
+            if (!ok) break;
+            reduce_rows<C, TE, 1>(acc, rg);
+            outputs(0);
+            if constexpr (NPASS == 2) {
+                head_pass<C, TE, JN>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qs, row0, hold);
+                reduce_rows<C, TE, 1>(acc, rg);
+                outputs(JN);
+            }
+        } else {
+            // GDN: per value column, the recurrence over the drafts.  The
+            // reductions keep all sums of one column in one lane: slots i < TMAX
+            // hold (S_c k_{m_i})[p], slots TMAX + i hold (S_c q_i)[p].
+            constexpr int HV = ilog2(VEC);
+            const int e = rg >> (LR - HV), pp = col0 + e;
+            const bool lead = (rg & ((1 << (LR - HV)) - 1)) == 0;
+            float sums[JP];
+            ok = head_pass<C, TE, 0>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qs, row0, hold);
+            if (!ok) break;
+            reduce_rows<C, TE, JN>(acc, rg);
+#pragma unroll
+            for (int t = 0; t < JN; ++t) sums[t] = acc[t];
+            if constexpr (NPASS >= 2) {
+                head_pass<C, TE, JN>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qs, row0, hold);
+                reduce_rows<C, TE, JN>(acc, rg);
+#pragma unroll
+                for (int t = 0; t < JN; ++t) sums[JN + t] = acc[t];
+            }
+            if constexpr (NPASS == 4) {
+                head_pass<C, TE, 2 * JN>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qs, row0, hold);
+                reduce_rows<C, TE, JN>(acc, rg);
+#pragma unroll
+                for (int t = 0; t < JN; ++t) sums[2 * JN + t] = acc[t];
+                head_pass<C, TE, 3 * JN>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qs, row0, hold);
+                reduce_rows<C, TE, JN>(acc, rg);
+#pragma unroll
+                for (int t = 0; t < JN; ++t) sums[3 * JN + t] = acc[t];
+            }
+            float ud[TMAX];
+#pragma unroll
+            for (int i = 0; i < TMAX; ++i) {
+                ud[i] = 0.f;
+                if (i < T) {
+                    const int m = hc + i;
+                    float sk = g1[j * TMAX + i] * sums[i] + pre1[(j * TMAX + i) * P + pp];
+                    const float *cc1 = c1 + (j * TMAX + i) * cap + hc;
+#pragma unroll
+                    for (int i3 = 0; i3 < TMAX; ++i3)
+                        if (i3 < i) sk = fmaf(cc1[i3], ud[i3], sk);
+                    const float u = bt[i * HU + j] * (bf2f(vb[((size_t)i * HU + j) * P + pp]) - ar[j * cap + m] * sk);
+                    ud[i] = u;
+                    float yv = g2[j * TMAX + i] * sums[TMAX + i] + pre2[(j * TMAX + i) * P + pp];
+                    const float *cc2 = c2 + (j * TMAX + i) * cap + hc;
+#pragma unroll
+                    for (int i3 = 0; i3 < TMAX; ++i3)
+                        if (i3 <= i) yv = fmaf(cc2[i3], ud[i3], yv);
+                    if (lead) {
+                        unew[((size_t)j * TMAX + i) * P + pp] = u;
+                        if (append) static_cast<float *>(p.buf_v)[(((size_t)b * cap + slot(m)) * H + hh) * P + pp] = u;
+                        p.y[(((size_t)b * T + i) * H + hh) * P + pp] = yv;
+                    }
+                }
+            }
+            __syncwarp();  // the new records' u of the warp's columns are in the context
+        }
+        if (hold) {
+            if (keep) gather_fold_coefs<C>(cfs, fs, fw, F, j, wcol0, lane);
+#pragma unroll 1
+            for (int rb = 0; rb < NCB; ++rb) {
+                const int q = q0 + rb;
+                if (keep)
+                    fold_block<C, TE>(p, stages + (size_t)(q % NS) * C::STAGE + lane_off, kraw, cfs, lcol, gF[j], F,
+                                      rb * RB + row0, col0, goff, materialize);
+                release_stage(empty, q, NS);
+            }
+        }
+    }
+    it += HU * NCB;
+    return ok;
+}
+
+// ---------------------------------------------------------------------------
+// Role loops.
+template <class C>
+__device__ __forceinline__ void prep_loop(const ReplayParams &p, uint8_t *sm, const RSmem &L, int units, int HU,
+                                          int NS) {
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bars);
+    uint64_t *cplan = bars + 2 * NS, *cfull = cplan + 2, *cempty = cfull + 2;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
+    const unsigned upseq = p.H / HU;
+    const int tp = threadIdx.x - C::PREP0;
+    int cu = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++cu) {
+        const int buf = cu & 1;
+        const bool ok = wait_or_abort(cempty + buf, ((cu >> 1) & 1) ^ 1, abort_flag, p.status);
+        if (named_sync_or(1, C::NPT, !ok)) return;  // the producer and every consumer warp are done with it
+        uint8_t *cx = sm + L.ctx0 + buf * L.ctx_bytes;
+        UnitHdr *hdr = reinterpret_cast<UnitHdr *>(cx + L.hdr);
+        const int b = u / upseq, h0 = (u % upseq) * HU;
+        if (tp == 0) {
+            // plan the unit from the sequence's pointers and take part in the pointer update
+            const SeqPlan s = plan_sequence(p, b);
+            arrive_and_update(p, s, b, upseq, (u % upseq) == 0);
+            hdr->s = s;
+            hdr->b = b;
+            hdr->h0 = h0;
+            mbar_arrive(cplan + buf);  // release: the producer may stream the unit
+        }
+        if (named_sync_or(1, C::NPT, false)) return;
+        const SeqPlan s = hdr->s;
+        if (s.work && !prep_unit<C>(p, sm, L, cx, s, b, h0, HU)) return;
+        if (named_sync_or(1, C::NPT, false)) return;  // the whole context is written
+        if (tp == 0) mbar_arrive(cfull + buf);
+    }
+}
+
+template <class C>
+__device__ __forceinline__ void consumer_loop(const ReplayParams &p, uint8_t *sm, const RSmem &L, int units, int HU,
+                                              int NS) {
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bars);
+    uint64_t *cfull = bars + 2 * NS + 2, *cempty = cfull + 2;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
+    const int lane = threadIdx.x & 31;
+    int it = 0, cu = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++cu) {
+        const int buf = cu & 1;
+        const bool ok = __all_sync(0xffffffffu, wait_or_abort(cfull + buf, (cu >> 1) & 1, abort_flag, p.status));
+        if (!ok) return;
+        const uint8_t *cx = sm + L.ctx0 + buf * L.ctx_bytes;
+        const UnitHdr hd = *reinterpret_cast<const UnitHdr *>(cx + L.hdr);
+        if (hd.s.work) {
+            const bool done = plan_reads_lp(p, hd.s)
+                                  ? consume_heads<C, uint16_t>(p, sm, L, cx, hd.s, hd.b, hd.h0, HU, NS, it)
+                                  : consume_heads<C, float>(p, sm, L, cx, hd.s, hd.b, hd.h0, HU, NS, it);
+            if (!done) return;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cempty + buf);  // this warp is done with the context
+    }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::NT, C::MIN_BLOCKS)
+    replay_pipe_kernel(const ReplayParams p, const __grid_constant__ CUtensorMap map_hp,
+                       const __grid_constant__ CUtensorMap map_lp, int units, int HU, int NS) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // the swizzle pattern is a function of the shared address: align the carve-up to 1024 bytes
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const RSmem L = replay_smem<C>(p.cap, HU, NS);
+    if (threadIdx.x == 0) {
+        uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bars);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(bars + s, 1);             // full: the producer's expect_tx arrival
+            mbar_init(bars + NS + s, C::NCW);   // empty: one arrival per consumer warp
+        }
+        uint64_t *pb = bars + 2 * NS;
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(pb + k, 1);               // context planned: the prep warps (read by the producer)
+            mbar_init(pb + 2 + k, 1);           // context full: the prep warps
+            mbar_init(pb + 4 + k, C::NCW + 1);  // context empty: every consumer warp and the producer
+        }
+        *reinterpret_cast<volatile int *>(sm + L.abort) = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5;
+    if (warp < C::NCW) {
+        consumer_loop<C>(p, sm, L, units, HU, NS);
+    } else if (warp == C::NCW) {
+        if (threadIdx.x == 32 * C::NCW) producer<C>(p, sm, L, units, HU, NS, &map_hp, &map_lp);
+    } else {
+        prep_loop<C>(p, sm, L, units, HU, NS);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side.
+
+// Tensor map of a checkpoint copy viewed as [slabs][N][P/CB][CB] with CB
+// elements = 128 bytes innermost; the box is one row block of one slab
+// (CB x P/CB x N*CB/P x 1: contiguous in HBM, N x 128 bytes), landing in shared
+// memory as 128-byte lines with the 128-byte swizzle.
+bool encode_slab_map(CUtensorMap *map, const void *base, bool bf16, int P, int N, long long slabs);
+
+// Launch shape: heads per unit, ring depth, CTAs per SM, shared memory.
+struct LaunchShape {
+    int HU, NS, per_sm, smem;
+};
+
+// Device limits used to size launches (queried once per device).
+struct DeviceLimits {
+    int sms, smem_per_sm, smem_per_block, reserved_per_block;
+};
+cudaError_t device_limits(DeviceLimits &d);
+
+template <class C>
+LaunchShape choose_shape(const ReplayParams &p, const DeviceLimits &dl) {
+    const int hpg = p.H / p.G;
+    static constexpr int kHU[] = {8, 4, 2, 1};
+    LaunchShape best = {0, 0, 0, 0};
+    // two CTAs per SM (one CTA's per-unit phases overlap the other's stream),
+    // at least four stages each; else one CTA per SM with a deeper ring
+    for (int tier = C::MIN_BLOCKS == 2 ? 2 : 1; tier >= 1 && best.HU == 0; --tier) {
+        const int budget = (tier == 2 ? dl.smem_per_sm / 2 - dl.reserved_per_block : dl.smem_per_block) - 1024;
+        // a held head keeps all its row blocks resident: at least one fp32 slab of stages
+        const int ns_max = tier == 2 ? 8 : 12, ns_min = C::P * 4 / 128 > 4 ? C::P * 4 / 128 : 4;
+        for (int HU : kHU) {
+            if (hpg % HU != 0) continue;
+#if defined(RS_FORCE_HU)
+            if (HU > RS_FORCE_HU) continue;
+#endif
+            const int other = replay_smem<C>(p.cap, HU, 0).total;
+            int ns = (budget - other) / C::STAGE;
+            if (ns > ns_max) ns = ns_max;
+            if (ns < ns_min) continue;
+#if defined(RS_FORCE_NS)
+            ns = RS_FORCE_NS;
+#endif
+            best = {HU, ns, tier, replay_smem<C>(p.cap, HU, ns).total + 1024};
+            break;
+        }
+    }
+    return best;
+}
+
+template <class C>
+cudaError_t launch_pipe(const ReplayParams &p, cudaStream_t stream) {
+    DeviceLimits dl;
+    cudaError_t e = device_limits(dl);
+    if (e != cudaSuccess) return e;
+    const LaunchShape sh = choose_shape<C>(p, dl);
+    if (sh.HU == 0) return cudaErrorInvalidConfiguration;
+    auto kern = replay_pipe_kernel<C>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dl.smem_per_block);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::NT, sh.smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    CUtensorMap map_hp, map_lp;
+    memset(&map_hp, 0, sizeof map_hp);
+    memset(&map_lp, 0, sizeof map_lp);
+    const long long slabs = (long long)p.B * p.H;
+    if (p.ckpt_hp && !encode_slab_map(&map_hp, p.ckpt_hp, false, C::P, C::N, slabs)) return cudaErrorInvalidValue;
+    if (p.ckpt_lp && !encode_slab_map(&map_lp, p.ckpt_lp, true, C::P, C::N, slabs)) return cudaErrorInvalidValue;
+    const int units = p.B * (p.H / sh.HU);
+    const int grid = units < dl.sms * per_sm ? units : dl.sms * per_sm;
+    kern<<<grid, C::NT, sh.smem, stream>>>(p, map_hp, map_lp, units, sh.HU, sh.NS);
+    return cudaGetLastError();
+}
+
+// Verify launches instantiate the draft-count buckets 1, 4 and 8.
+template <int KIND, int P, int N>
+cudaError_t dispatch_shape(const ReplayParams &p, cudaStream_t s) {
+    const int T = p.mode == MODE_VERIFY ? p.T : 1;
+    if (T <= 1) return launch_pipe<RCfg<KIND, P, N, 1>>(p, s);
+    if (T <= 4) return launch_pipe<RCfg<KIND, P, N, 4>>(p, s);
+    return launch_pipe<RCfg<KIND, P, N, 8>>(p, s);
+}
+
+}  // namespace cols
+}  // namespace rs
