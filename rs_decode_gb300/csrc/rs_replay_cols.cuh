@@ -121,11 +121,11 @@ struct UnitHdr {
 // Shared-memory carve-up, byte offsets from a 1024-byte aligned base (stages
 // first, so every stage is 1024-byte aligned as the swizzle requires).  The
 // unit context (ctx*, offsets within one context) is double-buffered; the
-// prep warps' scratch (d1, d2, sr, cst and the staged GDN u records xr) is not:
-// a fold gathers the value records it needs from global memory into the
+// prep warps' scratch (d1, d2, sr, cst) is not.  Value records (Mamba-2 x, GDN
+// u) are read from global memory where needed: a fold gathers them into the
 // consumer warps' scratch (fcf: fw_r v_r for the warp's P/NCW columns).
 struct RSmem {
-    int stages, bars, abort, d1, d2, sr, cst, xr, fcf, ctx0, ctx_bytes;
+    int stages, bars, abort, d1, d2, sr, cst, fcf, ctx0, ctx_bytes;
     int hdr, kraw, ar, vb, bt, c1, c2, g1, g2, fw, gF, pre1, pre2, qs, unew;  // within a context
     int total;
 };
@@ -145,7 +145,6 @@ __host__ __device__ inline RSmem replay_smem(int cap, int HU, int NS) {
     s.d2 = o;     o += GDN ? al16(cap * TMAX * 4) : 0;              // GDN k_r . q_i
     s.sr = o;     o += al16(HU * cap * 4);                          // Mamba-2 dt_r
     s.cst = o;    o += al16(2 * HU * 4);                            // Mamba-2 A_h, D_h
-    s.xr = o;     o += GDN ? al16(HU * cap * P * 4) : 0;            // GDN committed u (fp32) per record
     s.fcf = o;    o += al16(C::NCW * cap * (P / C::NCW) * 4);       // consumer warps' fold coefficients
     int c = 0;
     s.hdr = c;    c += al16((int)sizeof(UnitHdr));
@@ -443,7 +442,6 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
     float *sr = reinterpret_cast<float *>(sm + L.sr);
     float *cst = reinterpret_cast<float *>(sm + L.cst);      // A_h (HU), D_h (HU)
     uint16_t *kraw = reinterpret_cast<uint16_t *>(cx + L.kraw);
-    float *uf = reinterpret_cast<float *>(sm + L.xr);        // GDN committed u (fp32)
     float *ar = reinterpret_cast<float *>(cx + L.ar);
     uint16_t *vb = reinterpret_cast<uint16_t *>(cx + L.vb);
     float *bt = reinterpret_cast<float *>(cx + L.bt);
@@ -466,6 +464,18 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
     uint4 xv[8];
 #pragma unroll
     for (int t = 0; t < 8; ++t) xv[t] = x_task && t < nrec ? ld_u4(x_src(t)) : make_uint4(0u, 0u, 0u, 0u);
+    // GDN step-5 tasks (one head, 4 value columns): the committed u of the
+    // first 8 records, likewise loaded before the staging
+    constexpr int PC4 = P / 4;
+    const float *ubuf = static_cast<const float *>(p.buf_v);
+    auto u_src = [&](int task, int r) {
+        return ubuf + (((size_t)b * cap + slot(r)) * H + h0 + task / PC4) * P + 4 * (task % PC4);
+    };
+    const bool u_pre = KIND == RS_GDN && T > 0 && tp < HU * PC4;
+    float4 uv[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+        uv[t] = u_pre && t < hc ? *reinterpret_cast<const float4 *>(u_src(tp, t)) : make_float4(0.f, 0.f, 0.f, 0.f);
 
     // ---- 1. one batch of cp.async copies for every small operand of the unit
     {
@@ -489,13 +499,8 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
                 if (p.D) cp_async4(cst + HU + i2, p.D + h0 + i2);
                 else cst[HU + i2] = 0.f;
             }
-        } else {  // committed u (fp32); the drafts' v (bf16) and beta
-            constexpr int UC = P / 4, VC = P / 8;
-            for (int i2 = tp; i2 < HU * hc * UC; i2 += NPT) {
-                const int c = i2 % UC, r = (i2 / UC) % hc, hd = i2 / (UC * hc), hh = h0 + hd;
-                const float *src = static_cast<const float *>(p.buf_v) + (((size_t)b * cap + slot(r)) * H + hh) * P;
-                cp_async16(uf + ((size_t)hd * cap + r) * P + 4 * c, src + 4 * c);
-            }
+        } else {  // the drafts' v (bf16) and beta (the committed u are read where needed)
+            constexpr int VC = P / 8;
             for (int i2 = tp; i2 < T * HU * VC; i2 += NPT) {
                 const int c = i2 % VC, hd = (i2 / VC) % HU, i = i2 / (VC * HU);
                 cp_async16(vb + ((size_t)i * HU + hd) * P + 8 * c, p.v + (((size_t)b * T + i) * H + h0 + hd) * P + 8 * c);
@@ -699,25 +704,52 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
         }
         if (named_sync_or(1, NPT, false)) return false;
     }
-    // GDN: committed-record parts of S_{m_i-1} k_{m_i} and S_{m_i} q_i, four
-    // columns per task
+    // GDN: committed-record parts of S_{m_i-1} k_{m_i} and S_{m_i} q_i: one
+    // task per head and 4 columns, all drafts at once; the committed u come
+    // from global memory, 8 records' loads in flight at a time (the first
+    // task's first 8 were issued before the staging)
     if (KIND == RS_GDN && T > 0) {
-        constexpr int PC = P / 4;
-        for (int i2 = tp; i2 < HU * T * PC; i2 += NPT) {
-            const int pc = i2 % PC, i = (i2 / PC) % T, hd = i2 / (PC * T);
-            float s1[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
-            const float *cc1 = c1 + (hd * TMAX + i) * cap, *cc2 = c2 + (hd * TMAX + i) * cap;
-#pragma unroll 4
-            for (int r = 0; r < hc; ++r) {
-                const float4 u = *reinterpret_cast<const float4 *>(uf + ((size_t)hd * cap + r) * P + 4 * pc);
-                const float a1 = cc1[r], a2 = cc2[r];
-                s1[0] = fmaf(a1, u.x, s1[0]); s1[1] = fmaf(a1, u.y, s1[1]);
-                s1[2] = fmaf(a1, u.z, s1[2]); s1[3] = fmaf(a1, u.w, s1[3]);
-                s2[0] = fmaf(a2, u.x, s2[0]); s2[1] = fmaf(a2, u.y, s2[1]);
-                s2[2] = fmaf(a2, u.z, s2[2]); s2[3] = fmaf(a2, u.w, s2[3]);
+        for (int task = tp; task < HU * PC4; task += NPT) {
+            const int hd = task / PC4, pc = task % PC4;
+            float s1[TMAX][4], s2[TMAX][4];
+#pragma unroll
+            for (int i = 0; i < TMAX; ++i)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s1[i][e] = s2[i][e] = 0.f;
+            for (int r0 = 0; r0 < hc; r0 += 8) {
+                if (r0 > 0 || task != tp) {
+#pragma unroll
+                    for (int t = 0; t < 8; ++t)
+                        uv[t] = r0 + t < hc ? *reinterpret_cast<const float4 *>(u_src(task, r0 + t))
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const int r = r0 + t;
+                    if (r >= hc) break;
+                    const float u[4] = {uv[t].x, uv[t].y, uv[t].z, uv[t].w};
+#pragma unroll
+                    for (int i = 0; i < TMAX; ++i) {
+                        if (i < T) {
+                            const float a1 = c1[(hd * TMAX + i) * cap + r], a2 = c2[(hd * TMAX + i) * cap + r];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                s1[i][e] = fmaf(a1, u[e], s1[i][e]);
+                                s2[i][e] = fmaf(a2, u[e], s2[i][e]);
+                            }
+                        }
+                    }
+                }
             }
-            *reinterpret_cast<float4 *>(pre1 + (hd * TMAX + i) * P + 4 * pc) = make_float4(s1[0], s1[1], s1[2], s1[3]);
-            *reinterpret_cast<float4 *>(pre2 + (hd * TMAX + i) * P + 4 * pc) = make_float4(s2[0], s2[1], s2[2], s2[3]);
+#pragma unroll
+            for (int i = 0; i < TMAX; ++i) {
+                if (i < T) {
+                    *reinterpret_cast<float4 *>(pre1 + (hd * TMAX + i) * P + 4 * pc) =
+                        make_float4(s1[i][0], s1[i][1], s1[i][2], s1[i][3]);
+                    *reinterpret_cast<float4 *>(pre2 + (hd * TMAX + i) * P + 4 * pc) =
+                        make_float4(s2[i][0], s2[i][1], s2[i][2], s2[i][3]);
+                }
+            }
         }
         if (named_sync_or(1, NPT, false)) return false;
     }
