@@ -5,13 +5,14 @@
 // Two replay pipelines serve the two families (both persistent and
 // warp-specialised, both streaming the checkpoint with bulk copies into a
 // shared-memory ring):
-//   * Mamba-2 (rs::rows): the CTA's consumer warps split the key rows of each
-//     staged slab and combine their partial dots through shared memory; the
-//     per-unit operands are staged by the consumers themselves.
-//   * Gated DeltaNet (rs::cols): each consumer warp owns value columns and
-//     reduces with shuffles alone (the recurrence over drafts that gives u is
-//     then warp-local), and prep warps build each unit's context one unit
-//     ahead of the consumers.
+//   * Mamba-2 (rs::rows, up to 4 drafts): the CTA's consumer warps split the
+//     key rows of each staged slab and combine their partial dots through
+//     shared memory; the per-unit operands are staged by the consumers
+//     themselves.
+//   * Gated DeltaNet, and Mamba-2 rounds of 5..8 drafts (rs::cols): each
+//     consumer warp owns value columns and reduces with shuffles alone (the
+//     recurrence over drafts that gives u is then warp-local), and prep warps
+//     build each unit's context one unit ahead of the consumers.
 #include <mutex>
 
 #include "rs_replay_cols.cuh"
@@ -101,7 +102,12 @@ cudaError_t device_limits(DeviceLimits &d) {
 }  // namespace cols
 
 cudaError_t replay_launch_64x64(const ReplayParams &p, int kind, cudaStream_t s) {
-    if (kind == RS_MAMBA2) return rows::dispatch_shape<RS_MAMBA2, 64, 64, 128, 1, 2, 1>(p, s);
+    if (kind == RS_MAMBA2) {
+        const int T = p.mode == MODE_VERIFY ? p.T : 1;
+        if (T > 4) return cols::launch_pipe<cols::RCfg<RS_MAMBA2, 64, 64, 8>>(p, s);
+        if (T > 1) return rows::launch_shape<RS_MAMBA2, 64, 64, 128, 4, 1, 2, 1>(p, s);
+        return rows::launch_shape<RS_MAMBA2, 64, 64, 128, 1, 1, 2, 1>(p, s);
+    }
     return cols::dispatch_shape<RS_GDN, 64, 64>(p, s);
 }
 
