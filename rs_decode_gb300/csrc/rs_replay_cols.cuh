@@ -10,13 +10,15 @@
 //
 // Kernel structure: a persistent, warp-specialised pipeline with three roles.
 //   * Work unit = HU heads of one sequence that share one key group.
-//   * A producer warp (one elected lane) streams each unit's checkpoint slabs,
-//     once the prep warps have planned the unit, into a ring of NS shared-
+//   * A producer warp: one lane plans units ahead (reads a sequence's
+//     pointers, takes part in the pointer update); another streams each
+//     unit's checkpoint slabs, once the prep warps have taken up its plan,
+//     into a ring of NS shared-
 //     memory stages with tiled tensor copies (TMA) that complete on mbarriers.  A stage is one row block of a slab: 16 KiB of whole key rows
 //     (contiguous in HBM), stored with the 128-byte swizzle, so a slab takes
 //     P*sizeof(elem)/128 stages.
-//   * Three prep warps plan each unit from the sequence's pointers and build
-//     its context one unit ahead of the consumers, in a double buffer: they
+//   * Three prep warps build each unit's context one unit ahead of the
+//     consumers, in a double buffer: they
 //     stage every small operand (buffered records, the step's keys / queries
 //     / values, per-head constants) with cp.async, append the new records, and
 //     compute the key.query dots, the decay coefficients (product scans over
@@ -34,7 +36,7 @@
 // sits at l*128 + ((c ^ (l & 7)) << 4).  Each shared-memory phase of 8 lanes
 // reads chunks that land in 8 different bank groups (see WGeo).
 //
-// Per-sequence pointers (base, h, nd) are read once per unit by the prep warps;
+// Per-sequence pointers (base, h, nd) are read once per unit by the planner;
 // the last unit to have read them (an arrival counter) writes the new values,
 // so no second launch is needed.  Every wait is bounded: on a time-out the CTA
 // raises RS_DEV_TIMEOUT, drains its copies and returns.
@@ -63,12 +65,15 @@ struct RCfg {
     // k_{m_i} (slots 0..TMAX-1) and the queries q_i (slots TMAX..2TMAX-1)
     static constexpr int JP = (KIND == RS_GDN ? 2 : 1) * TMAX;
     static constexpr int STAGE = N * 128;                 // one row block: N lines of 128 bytes
-    static constexpr int QW = JP < 4 ? JP : 4;            // query floats per shared-memory vector
+    static constexpr int QW = JP % 4 == 0 ? 4 : (JP % 2 == 0 ? 2 : 1);  // query floats per shared-memory vector
     static constexpr int QC = JP / QW;                    // vectors per key row
     static constexpr int MIN_BLOCKS = 2;                  // two CTAs per SM
     // dot vectors per pass over a staged head: at most 64 partial sums per lane
     template <int VEC> static constexpr int jn() { return VEC * JP <= 64 ? JP : 64 / VEC; }
     static_assert(N % 8 == 0 && N <= 256, "a stage is one tensor box");
+    // the Mamba-2 output reduction halves down to single sums: a power-of-two bucket
+    static_assert(KIND == RS_GDN || (JP & (JP - 1)) == 0, "draft bucket");
+    static constexpr int JPP = JP <= 1 ? 1 : 2 << ilog2(JP - 1);  // JP rounded up to a power of two
 };
 
 // Where a consumer warp's lanes sit in a stage of element type TE.  A row of
@@ -123,14 +128,21 @@ struct UnitHdr {
 // unit context (ctx*, offsets within one context) is double-buffered; the
 // prep warps' scratch (d1, d2, sr, cst) is not.  Value records (Mamba-2 x, GDN
 // u) are read from global memory where needed: a fold gathers them into the
-// consumer warps' scratch (fcf: fw_r v_r for the warp's P/NCW columns).
+// consumer warps' scratch (fcf: fw_r v_r for the warp's P/NCW columns, for
+// fold_chunk(cap) records at a time).
 struct RSmem {
-    int stages, bars, abort, d1, d2, sr, cst, fcf, ctx0, ctx_bytes;
+    int stages, bars, plans, abort, d1, d2, sr, cst, fcf, ctx0, ctx_bytes;
     int hdr, kraw, ar, vb, bt, c1, c2, g1, g2, fw, gF, pre1, pre2, qs, unew;  // within a context
     int total;
 };
 
 __host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
+
+// Units the planner lane may plan ahead of the prep warps.
+constexpr int kPlanRing = 4;
+// Records whose fold coefficients a consumer warp gathers at a time: the whole
+// window when it is at most 16 records (one gather per folded head), else 8.
+__host__ __device__ inline int fold_chunk(int cap) { return cap <= 16 ? 16 : 8; }
 
 template <class C>
 __host__ __device__ inline RSmem replay_smem(int cap, int HU, int NS) {
@@ -139,13 +151,14 @@ __host__ __device__ inline RSmem replay_smem(int cap, int HU, int NS) {
     RSmem s;
     int o = 0;
     s.stages = o; o += NS * C::STAGE;
-    s.bars = o;   o += al16((2 * NS + 6) * 8);                      // stage and context barriers
+    s.bars = o;   o += al16((2 * NS + 6 + 2 * kPlanRing) * 8);      // stage, context and plan barriers
+    s.plans = o;  o += al16(kPlanRing * (int)sizeof(UnitHdr));
     s.abort = o;  o += 16;
     s.d1 = o;     o += al16(cap * TMAX * 4);                        // k_r . q_i (GDN: k_r . k_{m_i})
     s.d2 = o;     o += GDN ? al16(cap * TMAX * 4) : 0;              // GDN k_r . q_i
     s.sr = o;     o += al16(HU * cap * 4);                          // Mamba-2 dt_r
     s.cst = o;    o += al16(2 * HU * 4);                            // Mamba-2 A_h, D_h
-    s.fcf = o;    o += al16(C::NCW * cap * (P / C::NCW) * 4);       // consumer warps' fold coefficients
+    s.fcf = o;    o += al16(fold_chunk(cap) * P * 4);               // consumer warps' fold coefficients
     int c = 0;
     s.hdr = c;    c += al16((int)sizeof(UnitHdr));
     s.kraw = c;   c += al16((cap + TMAX) * N * 2);                  // bf16 keys (rows < cap), queries (cap + i)
@@ -205,9 +218,9 @@ __device__ __forceinline__ void load_q(const float *qs, int n, float (&qv)[JN]) 
             qv[4 * c] = f.x; qv[4 * c + 1] = f.y; qv[4 * c + 2] = f.z; qv[4 * c + 3] = f.w;
         } else if constexpr (QW == 2) {
             const float2 f = *reinterpret_cast<const float2 *>(src);
-            qv[0] = f.x; qv[1] = f.y;
+            qv[2 * c] = f.x; qv[2 * c + 1] = f.y;
         } else {
-            qv[0] = *src;
+            qv[c] = *src;
         }
     }
 }
@@ -268,6 +281,32 @@ __device__ __forceinline__ void reduce_rows(float (&acc)[WGeo<C, TE>::M], int rg
 }
 
 // ---------------------------------------------------------------------------
+// Planner (one lane of the producer warp): reads each unit's pointers, takes
+// part in the pointer update, and hands the plan to the prep warps through a
+// ring of kPlanRing slots, so that the pointer reads and the arrival atomic of
+// later units overlap the prep warps' work on the current one.
+template <class C>
+__device__ __forceinline__ void planner(const ReplayParams &p, uint8_t *sm, const RSmem &L, int units, int HU,
+                                        int NS) {
+    uint64_t *pfull = reinterpret_cast<uint64_t *>(sm + L.bars) + 2 * NS + 6, *pempty = pfull + kPlanRing;
+    UnitHdr *plans = reinterpret_cast<UnitHdr *>(sm + L.plans);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
+    const unsigned upseq = p.H / HU;
+    int cu = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++cu) {
+        const int slot = cu % kPlanRing;
+        if (!wait_or_abort(pempty + slot, ((cu / kPlanRing) & 1) ^ 1, abort_flag, p.status)) return;
+        const int b = u / upseq;
+        const SeqPlan s = plan_sequence(p, b);
+        arrive_and_update(p, s, b, upseq, (u % upseq) == 0);
+        plans[slot].s = s;
+        plans[slot].b = b;
+        plans[slot].h0 = (u % upseq) * HU;
+        mbar_arrive(pfull + slot);  // release: the plan is visible to the prep warps
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Producer: stream each unit's row blocks once the prep warps have planned it.
 template <class C>
 __device__ __forceinline__ void producer(const ReplayParams &p, uint8_t *sm, const RSmem &L, int units, int HU,
@@ -321,16 +360,18 @@ struct FoldSrc {
     int base, hc, cap;
 };
 
-// Gathers fw_r v_r[p] for r < F and the warp's WC = P/NCW value columns
-// (from column wcol0 on) into the warp's scratch cfs[r][WC], fp32.  All the
-// loads of a head are independent and issued together.
+// Gathers fw_r v_r[p] for records r0 .. r0+nr-1 and the warp's WC = P/NCW
+// value columns (from column wcol0 on) into the warp's scratch
+// cfs[r - r0][WC], fp32.  The loads of a chunk are independent and issued
+// together.
 template <class C>
-__device__ __forceinline__ void gather_fold_coefs(float *cfs, const FoldSrc &fs, const float *fw, int F, int j,
-                                                  int wcol0, int lane) {
+__device__ __forceinline__ void gather_fold_coefs(float *cfs, const FoldSrc &fs, const float *fw, int r0, int nr,
+                                                  int j, int wcol0, int lane) {
     constexpr int WC = C::P / C::NCW, Q = WC / 4;  // four columns per item
     constexpr int VSZ = C::KIND == RS_MAMBA2 ? 2 : 4;
-    for (int i = lane; i < F * Q; i += 32) {
-        const int r = i / Q, c4 = i % Q;
+    __syncwarp();  // the previous chunk's coefficients have been read
+    for (int i = lane; i < nr * Q; i += 32) {
+        const int r = r0 + i / Q, c4 = i % Q;
         int sl = fs.base + r;
         if (sl >= fs.cap) sl -= fs.cap;
         const uint8_t *src = (r < fs.hc ? fs.committed + (size_t)sl * fs.slot_stride
@@ -340,34 +381,23 @@ __device__ __forceinline__ void gather_fold_coefs(float *cfs, const FoldSrc &fs,
         if constexpr (C::KIND == RS_MAMBA2) load_bf16_vec<4>(reinterpret_cast<const uint16_t *>(src), v);
         else load_f32_vec<4>(reinterpret_cast<const float *>(src), v);
         const float w = fw[j * fs.cap + r];
-        *reinterpret_cast<float4 *>(cfs + r * WC + 4 * c4) = make_float4(w * v[0], w * v[1], w * v[2], w * v[3]);
+        *reinterpret_cast<float4 *>(cfs + (r - r0) * WC + 4 * c4) =
+            make_float4(w * v[0], w * v[1], w * v[2], w * v[3]);
     }
     __syncwarp();
 }
 
-// Fold of the lane's columns of one staged row block:
-//   S_new = gF S_c + sum_{r<F} (fw_r v_r) k_r^T
-// written to the checkpoint (both copies as present) or to the materialise
-// output.  The coefficients fw_r v_r come from the warp's scratch (lane
-// columns from lcol on); each is applied to the lane's RK rows (row0, row0 +
-// RGW, ...).
+// Adds records r0 .. r0+nr-1 of the fold S_new = gF S_c + sum_r (fw_r v_r) k_r^T
+// to the lane's RK rows (row0, row0 + RGW, ...) of one row block: o[k][e].
 template <class C, typename TE>
-__device__ __forceinline__ void fold_block(const ReplayParams &p, const uint8_t *lane_base, const uint16_t *kraw,
-                                           const float *cfs, int lcol, float gf, int F, int row0, int col0,
-                                           size_t goff, bool materialize) {
+__device__ __forceinline__ void fold_records(float (&o)[WGeo<C, TE>::RK][WGeo<C, TE>::VEC], const uint16_t *kraw,
+                                             const float *cfs, int lcol, int r0, int nr, int row0) {
     using W = WGeo<C, TE>;
-    constexpr int VEC = W::VEC, RK = W::RK, RGW = W::RGW, N = C::N, P = C::P, WC = C::P / C::NCW;
-    float o[RK][VEC];
-#pragma unroll
-    for (int k = 0; k < RK; ++k) {
-        unpack<TE, VEC>(ld_u4(lane_base + (size_t)k * RGW * W::NCB * 128), o[k]);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) o[k][e] *= gf;
-    }
-    for (int r = 0; r < F; ++r) {
+    constexpr int VEC = W::VEC, RK = W::RK, RGW = W::RGW, N = C::N, WC = C::P / C::NCW;
+    for (int r = 0; r < nr; ++r) {
         float cf[VEC];
         load_f32_vec<VEC>(cfs + r * WC + lcol, cf);
-        const uint16_t *kr = kraw + (size_t)r * N + row0;
+        const uint16_t *kr = kraw + (size_t)(r0 + r) * N + row0;
 #pragma unroll
         for (int k = 0; k < RK; ++k) {
             const float kv = bf2f(kr[k * RGW]);
@@ -375,6 +405,15 @@ __device__ __forceinline__ void fold_block(const ReplayParams &p, const uint8_t 
             for (int e = 0; e < VEC; ++e) o[k][e] = fmaf(cf[e], kv, o[k][e]);
         }
     }
+}
+
+// Writes the folded rows of one row block: the checkpoint (both copies as
+// present) or the materialise output.
+template <class C, typename TE>
+__device__ __forceinline__ void fold_store(const ReplayParams &p, const float (&o)[WGeo<C, TE>::RK][WGeo<C, TE>::VEC],
+                                           int row0, int col0, size_t goff, bool materialize) {
+    using W = WGeo<C, TE>;
+    constexpr int VEC = W::VEC, RK = W::RK, RGW = W::RGW, P = C::P;
 #pragma unroll
     for (int k = 0; k < RK; ++k) {
         const size_t off = goff + (size_t)(row0 + k * RGW) * P + col0;
@@ -383,6 +422,66 @@ __device__ __forceinline__ void fold_block(const ReplayParams &p, const uint8_t 
         } else {
             if (p.ckpt_hp) store_f32<VEC>(p.ckpt_hp + off, o[k]);
             if (p.ckpt_lp) store_bf16<VEC>(p.ckpt_lp + off, o[k]);
+        }
+    }
+}
+
+// Fold of the lane's columns of a head whose NCB row blocks are all staged.
+// Coefficients are gathered fc records at a time.  fp32 blocks keep
+// the partial sums in place between chunks (each lane rewrites only its own
+// elements), so each chunk is gathered once per head; bf16 blocks (shared-bf16
+// checkpoints) keep them in registers, one row block at a time.
+template <class C, typename TE>
+__device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages, int lane_off, int q0, int NS,
+                                          const uint16_t *kraw,
+                                          float *cfs, const FoldSrc &fs, const float *fw, float gf, int F, int j,
+                                          int row0, int col0, int wcol0, int lcol, size_t goff, bool materialize,
+                                          int lane, int fc) {
+    using W = WGeo<C, TE>;
+    constexpr int VEC = W::VEC, RK = W::RK, RGW = W::RGW, NCB = W::NCB, RB = W::RB;
+    constexpr size_t RSTEP = (size_t)RGW * NCB * 128;
+    const int nch = F > 0 ? (F + fc - 1) / fc : 1;
+    auto blk = [&](int rb) { return stages + (size_t)((q0 + rb) % NS) * C::STAGE + lane_off; };
+    if constexpr (sizeof(TE) == 4) {
+        for (int c = 0; c < nch; ++c) {
+            const int r0 = c * fc, nr = F - r0 < fc ? F - r0 : fc;
+            gather_fold_coefs<C>(cfs, fs, fw, r0, nr > 0 ? nr : 0, j, wcol0, lane);
+            for (int rb = 0; rb < NCB; ++rb) {
+                float o[RK][VEC];
+#pragma unroll
+                for (int k = 0; k < RK; ++k) {
+                    unpack<TE, VEC>(ld_u4(blk(rb) + k * RSTEP), o[k]);
+                    if (c == 0)
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) o[k][e] *= gf;
+                }
+                fold_records<C, TE>(o, kraw, cfs, lcol, r0, nr > 0 ? nr : 0, rb * RB + row0);
+                if (c == nch - 1) {
+                    fold_store<C, TE>(p, o, rb * RB + row0, col0, goff, materialize);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < RK; ++k)
+                        *reinterpret_cast<float4 *>(blk(rb) + k * RSTEP) = make_float4(o[k][0], o[k][1], o[k][2], o[k][3]);
+                }
+            }
+        }
+        // the partial sums written into the stages precede the next copies into them
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    } else {
+        for (int rb = 0; rb < NCB; ++rb) {
+            float o[RK][VEC];
+#pragma unroll
+            for (int k = 0; k < RK; ++k) {
+                unpack<TE, VEC>(ld_u4(blk(rb) + k * RSTEP), o[k]);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) o[k][e] *= gf;
+            }
+            for (int c = 0; c < nch; ++c) {
+                const int r0 = c * fc, nr = F - r0 < fc ? F - r0 : fc;
+                gather_fold_coefs<C>(cfs, fs, fw, r0, nr > 0 ? nr : 0, j, wcol0, lane);
+                fold_records<C, TE>(o, kraw, cfs, lcol, r0, nr > 0 ? nr : 0, rb * RB + row0);
+            }
+            fold_store<C, TE>(p, o, rb * RB + row0, col0, goff, materialize);
         }
     }
 }
@@ -552,51 +651,75 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
         }
         // (Mamba-2: the new records' x are appended by the step-5 tasks)
     }
+    // the key row that holds dot-vector slot jj: Mamba-2 C_jj; GDN k_{hc+jj}
+    // (jj < TMAX) or q_{jj-TMAX}; -1 for the slots past the launch's drafts
+    auto slot_row = [&](int jj) {
+        if (KIND == RS_MAMBA2) return jj < T ? cap + jj : -1;
+        if (jj < TMAX) return jj < T ? hc + jj : -1;
+        return jj - TMAX < T ? cap + jj - TMAX : -1;
+    };
     if (T > 0) {
-        // slot jj of row n: Mamba-2 C_jj; GDN k_{hc+jj} (jj < TMAX) or q_{jj-TMAX};
-        // slots past the launch's drafts are zero
-        for (int i2 = tp; i2 < N * JP; i2 += NPT) {
-            const int n = i2 % N, jj = i2 / N;
-            int row = -1;
-            if (KIND == RS_MAMBA2) {
-                if (jj < T) row = cap + jj;
-            } else if (jj < TMAX) {
-                if (jj < T) row = hc + jj;
-            } else if (jj - TMAX < T) {
-                row = cap + jj - TMAX;
+        // one key row n per task: its JP slots as fp32, QW at a time
+        for (int n = tp; n < N; n += NPT) {
+#pragma unroll
+            for (int c = 0; c < C::QC; ++c) {
+                float v[C::QW];
+#pragma unroll
+                for (int w = 0; w < C::QW; ++w) {
+                    const int row = slot_row(c * C::QW + w);
+                    v[w] = row >= 0 ? bf2f(kraw[(size_t)row * N + n]) : 0.f;
+                }
+                float *dst = qs + ((size_t)c * N + n) * C::QW;
+                if constexpr (C::QW == 4) *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+                else if constexpr (C::QW == 2) *reinterpret_cast<float2 *>(dst) = make_float2(v[0], v[1]);
+                else dst[0] = v[0];
             }
-            qs[((size_t)(jj / C::QW) * N + n) * C::QW + jj % C::QW] = row >= 0 ? bf2f(kraw[(size_t)row * N + n]) : 0.f;
         }
     }
 
-    // ---- 3. key/query dot products of the group (8 lanes per dot)
+    // ---- 3. key . dot-vector products d(r, jj) = k_r . v_jj (Mamba-2: d1 = k_r . q_i;
+    // GDN: d1 = k_r . k_{m_i}, d2 = k_r . q_i): one warp per record at a time,
+    // lane = key rows lane + 32 t; the slot vectors are read once per warp
+    // from the staged bf16 rows, then a recursive-halving warp reduction
+    // leaves slot jj's sum in lanes jj << (5 - log2 JP)
     if (T > 0) {
-        const int per = nrec * T;
-        const int ndots = (KIND == RS_GDN ? 2 : 1) * per;
-        for (int bd = 0; bd < ndots; bd += NPT / 8) {
-            const int d = bd + tp / 8, sub = tp % 8;
-            float acc = 0.f;
-            int r = 0, i = 0, which = 0;
-            if (d < ndots) {
-                which = d / per;
-                r = (d % per) / T;
-                i = d % T;
-                const uint16_t *a = kraw + (size_t)r * N;
-                // Mamba-2: k_r . q_i ; GDN which 0: k_r . k_{hc+i}, which 1: k_r . q_i
-                const uint16_t *bv = (KIND == RS_GDN && which == 0) ? kraw + (size_t)(hc + i) * N
-                                                                    : kraw + (size_t)(cap + i) * N;
-                for (int n = sub * 8; n < N; n += 64) {
-                    float fa[8], fb[8];
-                    unpack<uint16_t, 8>(ld_u4(a + n), fa);
-                    unpack<uint16_t, 8>(ld_u4(bv + n), fb);
+        constexpr int JPP = C::JPP, NPL = N / 32, LJ = ilog2(JPP);  // padded to a power of two
+        constexpr bool HOIST = NPL * JPP <= 32;
+        float qv[HOIST ? NPL : 1][JPP];
+        auto slot_vals = [&](int t, float (&v)[JPP]) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc = fmaf(fa[e], fb[e], acc);
+            for (int jj = 0; jj < JPP; ++jj) {
+                const int row = jj < JP ? slot_row(jj) : -1;
+                v[jj] = row >= 0 ? bf2f(kraw[(size_t)row * N + lane + 32 * t]) : 0.f;
+            }
+        };
+        if constexpr (HOIST) {
+#pragma unroll
+            for (int t = 0; t < NPL; ++t) slot_vals(t, qv[t]);
+        }
+        for (int r = pw; r < nrec; r += C::NPW) {
+            float acc[JPP];
+#pragma unroll
+            for (int jj = 0; jj < JPP; ++jj) acc[jj] = 0.f;
+#pragma unroll
+            for (int t = 0; t < NPL; ++t) {
+                const float kv = bf2f(kraw[(size_t)r * N + lane + 32 * t]);
+                if constexpr (!HOIST) slot_vals(t, qv[0]);
+#pragma unroll
+                for (int jj = 0; jj < JPP; ++jj) acc[jj] = fmaf(kv, qv[HOIST ? t : 0][jj], acc[jj]);
+            }
+            RowReduce<JPP, JPP, 1, 16, 0>::run(acc, lane);
+            const int sh = 5 - LJ;
+            if ((lane & ((1 << sh) - 1)) == 0) {
+                const int jj = lane >> sh;
+                if (KIND == RS_MAMBA2) {
+                    if (jj < T) d1[r * TMAX + jj] = acc[0];
+                } else if (jj < TMAX) {
+                    if (jj < T) d1[r * TMAX + jj] = acc[0];
+                } else if (jj - TMAX < T) {
+                    d2[r * TMAX + jj - TMAX] = acc[0];
                 }
             }
-            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-            if (d < ndots && sub == 0) (which == 0 ? d1 : d2)[r * TMAX + i] = acc;
         }
     }
     if (named_sync_or(1, NPT, false)) return false;
@@ -800,7 +923,8 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
     const int lane_off = line0 * 128 + ((ch ^ (line0 & 7)) << 4);
     // the warp's value columns are contiguous: P / NCW of them from wcol0
     const int wcol0 = cb * W::CBE + (warp % W::WPC) * W::CPW * VEC, lcol = col0 - wcol0;
-    float *cfs = reinterpret_cast<float *>(sm + L.fcf) + (size_t)warp * cap * (P / C::NCW);
+    const int fc = fold_chunk(cap);
+    float *cfs = reinterpret_cast<float *>(sm + L.fcf) + (size_t)warp * fc * (P / C::NCW);
     // A head stays resident (all its row blocks) when the slab is read again
     // after the reduction: by further passes, or by the fold (which for GDN
     // takes in the u this launch computes).  Otherwise each row block is
@@ -823,16 +947,12 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
             fs.fresh_stride = (size_t)P * 4;
         }
         fs.base = base; fs.hc = hc; fs.cap = cap;
-        if (T == 0) {  // flush / materialise: fold only
-            gather_fold_coefs<C>(cfs, fs, fw, F, j, wcol0, lane);
-#pragma unroll 1
-            for (int rb = 0; rb < NCB; ++rb) {
-                const int q = q0 + rb;
-                if (!(ok = wait_stage(full, q, NS, abort_flag, p.status, ok))) break;
-                fold_block<C, TE>(p, stages + (size_t)(q % NS) * C::STAGE + lane_off, kraw, cfs, lcol, gF[j], F,
-                                  rb * RB + row0, col0, goff, materialize);
-                release_stage(empty, q, NS);
-            }
+        if (T == 0) {  // flush / materialise: fold only, the head's row blocks all resident
+            for (int rb = 0; rb < NCB && ok; ++rb) ok = wait_stage(full, q0 + rb, NS, abort_flag, p.status, ok);
+            if (!ok) break;
+            fold_head<C, TE>(p, const_cast<uint8_t *>(stages), lane_off, q0, NS, kraw, cfs, fs, fw, gF[j], F, j,
+                             row0, col0, wcol0, lcol, goff, materialize, lane, fc);
+            for (int rb = 0; rb < NCB; ++rb) release_stage(empty, q0 + rb, NS);
             continue;
         }
         if (hold)
@@ -922,15 +1042,10 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
             __syncwarp();  // the new records' u of the warp's columns are in the context
         }
         if (hold) {
-            if (keep) gather_fold_coefs<C>(cfs, fs, fw, F, j, wcol0, lane);
-#pragma unroll 1
-            for (int rb = 0; rb < NCB; ++rb) {
-                const int q = q0 + rb;
-                if (keep)
-                    fold_block<C, TE>(p, stages + (size_t)(q % NS) * C::STAGE + lane_off, kraw, cfs, lcol, gF[j], F,
-                                      rb * RB + row0, col0, goff, materialize);
-                release_stage(empty, q, NS);
-            }
+            if (keep)
+                fold_head<C, TE>(p, const_cast<uint8_t *>(stages), lane_off, q0, NS, kraw, cfs, fs, fw, gF[j], F, j,
+                                 row0, col0, wcol0, lcol, goff, materialize, lane, fc);
+            for (int rb = 0; rb < NCB; ++rb) release_stage(empty, q0 + rb, NS);
         }
     }
     it += HU * NCB;
@@ -944,6 +1059,8 @@ __device__ __forceinline__ void prep_loop(const ReplayParams &p, uint8_t *sm, co
                                           int NS) {
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bars);
     uint64_t *cplan = bars + 2 * NS, *cfull = cplan + 2, *cempty = cfull + 2;
+    uint64_t *pfull = cempty + 2, *pempty = pfull + kPlanRing;
+    const UnitHdr *plans = reinterpret_cast<const UnitHdr *>(sm + L.plans);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
     const unsigned upseq = p.H / HU;
     const int tp = threadIdx.x - C::PREP0;
@@ -956,15 +1073,16 @@ __device__ __forceinline__ void prep_loop(const ReplayParams &p, uint8_t *sm, co
         UnitHdr *hdr = reinterpret_cast<UnitHdr *>(cx + L.hdr);
         const int b = u / upseq, h0 = (u % upseq) * HU;
         if (tp == 0) {
-            // plan the unit from the sequence's pointers and take part in the pointer update
-            const SeqPlan s = plan_sequence(p, b);
-            arrive_and_update(p, s, b, upseq, (u % upseq) == 0);
-            hdr->s = s;
-            hdr->b = b;
-            hdr->h0 = h0;
-            mbar_arrive(cplan + buf);  // release: the producer may stream the unit
+            // the unit's plan, from the planner lane
+            const int slot = cu % kPlanRing;
+            const bool got = wait_or_abort(pfull + slot, (cu / kPlanRing) & 1, abort_flag, p.status);
+            if (got) {
+                *hdr = plans[slot];
+                mbar_arrive(pempty + slot);
+                mbar_arrive(cplan + buf);  // release: the producer may stream the unit
+            }
         }
-        if (named_sync_or(1, C::NPT, false)) return;
+        if (named_sync_or(1, C::NPT, *abort_flag != 0)) return;
         const SeqPlan s = hdr->s;
         if (s.work && !prep_unit<C>(p, sm, L, cx, s, b, h0, HU)) return;
         if (named_sync_or(1, C::NPT, false)) return;  // the whole context is written
@@ -1017,6 +1135,10 @@ __global__ void __launch_bounds__(C::NT, C::MIN_BLOCKS)
             mbar_init(pb + 2 + k, 1);           // context full: the prep warps
             mbar_init(pb + 4 + k, C::NCW + 1);  // context empty: every consumer warp and the producer
         }
+        for (int k = 0; k < kPlanRing; ++k) {
+            mbar_init(pb + 6 + k, 1);               // plan full: the planner lane
+            mbar_init(pb + 6 + kPlanRing + k, 1);   // plan empty: the prep warps
+        }
         *reinterpret_cast<volatile int *>(sm + L.abort) = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -1026,6 +1148,7 @@ __global__ void __launch_bounds__(C::NT, C::MIN_BLOCKS)
         consumer_loop<C>(p, sm, L, units, HU, NS);
     } else if (warp == C::NCW) {
         if (threadIdx.x == 32 * C::NCW) producer<C>(p, sm, L, units, HU, NS, &map_hp, &map_lp);
+        else if (threadIdx.x == 32 * C::NCW + 1) planner<C>(p, sm, L, units, HU, NS);
     } else {
         prep_loop<C>(p, sm, L, units, HU, NS);
     }
@@ -1111,11 +1234,12 @@ cudaError_t launch_pipe(const ReplayParams &p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-// Verify launches instantiate the draft-count buckets 1, 4 and 8.
+// Verify launches instantiate the draft-count buckets 1, 4 and 8 (GDN also 3).
 template <int KIND, int P, int N>
 cudaError_t dispatch_shape(const ReplayParams &p, cudaStream_t s) {
     const int T = p.mode == MODE_VERIFY ? p.T : 1;
     if (T <= 1) return launch_pipe<RCfg<KIND, P, N, 1>>(p, s);
+    if (KIND == RS_GDN && T <= 3) return launch_pipe<RCfg<KIND, P, N, 3>>(p, s);
     if (T <= 4) return launch_pipe<RCfg<KIND, P, N, 4>>(p, s);
     return launch_pipe<RCfg<KIND, P, N, 8>>(p, s);
 }
