@@ -85,7 +85,7 @@ __host__ __device__ inline PipeSmem pipe_smem(int cap) {
     s.g2 = o;     o += al16(HU * TMAX * 4);
     s.fw = o;     o += al16(HU * cap * 4);
     s.gF = o;     o += al16(HU * 4);
-    s.pre1 = o;   o += GDN ? al16(HU * TMAX * P * 4) : 0;
+    s.pre1 = o;   o += al16(HU * TMAX * P * 4);                     // record parts of the outputs
     s.pre2 = o;   o += GDN ? al16(HU * TMAX * P * 4) : 0;
     s.red = o;    o += al16(2 * C::NCW * C::JMAX * P * 4);          // double-buffered warp partials
     s.total = o;
@@ -390,49 +390,84 @@ __device__ __forceinline__ bool consume_unit(const ReplayParams &p, uint8_t *sm,
     //            c2[i][r] = E(r, m_i) (k_r . q_i)          (r <= m_i) -> S_{m_i} q_i
     //            g1[i] = gamma(m_i - 1), g2[i] = gamma(m_i)
     //   fold of F records: fw[r] = E(r, F-1) (times dt_r for Mamba-2), gF = gamma(F-1)
-    {
-        const int nA = HU * T * nrec;
-        for (int i2 = tid; i2 < nA + HU * T + HU * F + HU; i2 += NC) {
-            if (i2 < nA) {
-                const int r = i2 % nrec, i = (i2 / nrec) % T, hd = i2 / (nrec * T);
-                const float *a = ar + hd * cap;
-                const int m = hc + i;
-                float e = 1.f;  // E(r, m - 1)
-                for (int q = r + 1; q <= m - 1; ++q) e *= a[q];
-                const float em = r == m ? 1.f : e * a[m];  // E(r, m)
-                float v1 = 0.f, v2 = 0.f;
+    // One warp per head, one lane per record: a reverse product scan of
+    // v_s = (s < hc ? alpha_s : 1) gives E(r, hc-1) in lane r and gamma(hc-1)
+    // in lane 0; each further bound m (up to hc+T-1; F-1 is among them) takes
+    // one more factor: E(r, m) = E(r, m-1) alpha_m for r < m, E(m, m) = 1.
+    for (int hd = warp; hd < HU; hd += NCW) {
+        const float al = lane < nrec ? ar[hd * cap + lane] : 1.f;
+        const float dtr = KIND == RS_MAMBA2 && lane < nrec ? sr[hd * cap + lane] : 1.f;
+        float inc = lane < hc ? al : 1.f;  // inclusive: prod_{s >= lane} v_s
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float o = __shfl_down_sync(0xffffffffu, inc, off);
+            if (lane + off < 32) inc *= o;
+        }
+        float E = __shfl_down_sync(0xffffffffu, inc, 1);  // prod_{s > lane} v_s = E(lane, hc-1)
+        if (lane == 31) E = 1.f;
+        float gam = __shfl_sync(0xffffffffu, inc, 0);  // gamma(hc-1)
+        for (int m = hc - 1; m < hc + T; ++m) {
+            if (m >= hc) {
+                const float am = __shfl_sync(0xffffffffu, al, m);  // alpha_m (m < nrec <= 32)
+                E = lane < m ? E * am : 1.f;
+                gam *= am;
+            }
+            const int i = m - hc;  // the draft whose own position is m (-1: none)
+            if (lane < nrec) {
                 if (KIND == RS_MAMBA2) {
-                    if (r <= m) v1 = em * sr[hd * cap + r] * d1[r * TMAX + i];
+                    if (i >= 0) c1[(hd * TMAX + i) * cap + lane] = lane <= m ? E * dtr * d1[lane * TMAX + i] : 0.f;
                 } else {
-                    if (r < m) v1 = e * d1[r * TMAX + i];
-                    if (r <= m) v2 = em * d2[r * TMAX + i];
+                    if (i >= 0) c2[(hd * TMAX + i) * cap + lane] = lane <= m ? E * d2[lane * TMAX + i] : 0.f;
+                    if (i + 1 < T) c1[(hd * TMAX + i + 1) * cap + lane] = lane <= m ? E * d1[lane * TMAX + i + 1] : 0.f;
                 }
-                c1[(hd * TMAX + i) * cap + r] = v1;
-                c2[(hd * TMAX + i) * cap + r] = v2;
-            } else if (i2 < nA + HU * T) {
-                const int j = i2 - nA, i = j % T, hd = j / T;
-                const float *a = ar + hd * cap;
-                const int m = hc + i;
-                float e = 1.f;
-                for (int q = 0; q < m; ++q) e *= a[q];
-                g1[hd * TMAX + i] = KIND == RS_MAMBA2 ? e * a[m] : e;
-                g2[hd * TMAX + i] = e * a[m];
-            } else if (i2 < nA + HU * T + HU * F) {
-                const int j = i2 - nA - HU * T, r = j % F, hd = j / F;
-                const float *a = ar + hd * cap;
-                float e = 1.f;
-                for (int q = r + 1; q < F; ++q) e *= a[q];
-                fw[hd * cap + r] = KIND == RS_MAMBA2 ? e * sr[hd * cap + r] : e;
-            } else {
-                const int hd = i2 - nA - HU * T - HU * F;
-                const float *a = ar + hd * cap;
-                float e = 1.f;
-                for (int q = 0; q < F; ++q) e *= a[q];
-                gF[hd] = e;
+                if (m == F - 1 && lane < F) fw[hd * cap + lane] = KIND == RS_MAMBA2 ? E * dtr : E;
+            }
+            if (lane == 0) {
+                if (i >= 0) {
+                    if (KIND == RS_MAMBA2) g1[hd * TMAX + i] = gam;
+                    else g2[hd * TMAX + i] = gam;
+                }
+                if (KIND == RS_GDN && i + 1 < T) g1[hd * TMAX + i + 1] = gam;
+                if (m == F - 1) gF[hd] = gam;
             }
         }
+        if (F == 0 && lane == 0) gF[hd] = 1.f;
     }
     if (named_sync_or(1, NC, false)) return false;
+
+    // ---- 5 (Mamba-2): record parts of the outputs, rec_i[p] = sum_{r <= m_i} c1[i][r] x_r[p]
+    // + D x_{m_i}[p]; one task per head and 4 columns, all drafts at once
+    if (KIND == RS_MAMBA2 && T > 0) {
+        constexpr int PC = P / 4;
+        for (int i2 = tid; i2 < HU * PC; i2 += NC) {
+            const int pc = i2 % PC, hd = i2 / PC;
+            const float d = cst[HU + hd];
+            float a[TMAX][4];
+#pragma unroll
+            for (int i = 0; i < TMAX; ++i)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) a[i][e] = 0.f;
+            const uint16_t *xr = xb + (size_t)hd * cap * P + 4 * pc;
+            for (int r = 0; r < nrec; ++r) {
+                float xv[4];
+                load_bf16_run<4>(xr + (size_t)r * P, xv);
+#pragma unroll
+                for (int i = 0; i < TMAX; ++i) {
+                    if (i < T && r <= hc + i) {
+                        const float c = c1[(hd * TMAX + i) * cap + r] + (r == hc + i ? d : 0.f);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) a[i][e] = fmaf(c, xv[e], a[i][e]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < TMAX; ++i)
+                if (i < T)
+                    *reinterpret_cast<float4 *>(pre1 + (hd * TMAX + i) * P + 4 * pc) =
+                        make_float4(a[i][0], a[i][1], a[i][2], a[i][3]);
+        }
+        // read after the first head's partial barrier
+    }
 
     // ---- 5 (GDN): committed-record parts of S_{m_i-1} k_{m_i} and S_{m_i} q_i
     if (KIND == RS_GDN && T > 0) {
@@ -518,18 +553,13 @@ __device__ __forceinline__ bool consume_unit(const ReplayParams &p, uint8_t *sm,
         if (named_sync_or(1, NC, !ok)) return false;  // partials of head j complete
 
         if (KIND == RS_MAMBA2) {
-            // y_i[p] = gamma(m_i) (S_c q_i)[p] + sum_r c1[i][r] x_r[p] + D x_{m_i}[p]
+            // y_i[p] = gamma(m_i) (S_c q_i)[p] + rec_i[p]
             for (int i2 = tid; i2 < T * P; i2 += NC) {
-                const int i = i2 / P, pp = i2 % P, m = hc + i;
+                const int i = i2 / P, pp = i2 % P;
                 float sq = 0.f;
 #pragma unroll
                 for (int w = 0; w < NCW; ++w) sq += rb[((size_t)w * JMAX + i) * P + pp];
-                float yv = g1[j * TMAX + i] * sq;
-                const float *cc = c1 + (j * TMAX + i) * cap;
-                const uint16_t *xr = xb + (size_t)j * cap * P + pp;
-                for (int r = 0; r <= m; ++r) yv = fmaf(cc[r], bf2f(xr[(size_t)r * P]), yv);
-                yv = fmaf(cst[HU + j], bf2f(xr[(size_t)m * P]), yv);
-                p.y[(((size_t)b * T + i) * H + hh) * P + pp] = yv;
+                p.y[(((size_t)b * T + i) * H + hh) * P + pp] = fmaf(g1[j * TMAX + i], sq, pre1[(j * TMAX + i) * P + pp]);
             }
         } else {
             // GDN: per value index, the recurrence over the drafts
