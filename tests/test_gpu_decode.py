@@ -143,3 +143,27 @@ def test_append_then_decode():
         y = layer.decode(to_device(d), gp).cpu().numpy()
         assert rel_err(y, model.step(d)).max() <= TOL_HP
     assert layer.status() == 0
+
+
+@pytest.mark.parametrize("precision", ["fp32", "shared_bf16"])
+def test_gdn_long_window(precision):
+    """GDN with a 32-record window: a fold takes the coefficients of its 32
+    records in several gathers (fp32 checkpoints keep the partial sums in the
+    staged blocks between gathers, bf16 ones in registers)."""
+    w = synth.WORKLOADS["gdn"].with_(B=3, L=32)
+    _run_standard(w, 40, seed=11, precision=precision, check_materialize=(precision == "fp32"))
+
+
+def test_gdn_forced_flush_and_materialize():
+    """rs_flush and rs_materialize on GDN layers (fold-only launches)."""
+    w = synth.WORKLOADS["gdn"].with_(B=2)
+    run = StandardRun(w, seed=12)
+    for s in range(21):
+        y, y_ref, _ = run.step()
+        assert rel_err(y, y_ref).max() <= TOL_HP
+        if s in (3, 11, 12):
+            run.layer.flush()
+            run.ptr.flush()
+            assert (run.layer.pointers()["h"] == 0).all()
+            assert rel_err(run.checkpoint(), run.model.S).max() <= TOL_HP
+    assert rel_err(run.materialized(), run.model.S).max() <= TOL_HP

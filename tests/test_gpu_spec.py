@@ -126,3 +126,10 @@ def test_bad_accept_sets_status_bit():
     assert run.layer.status() & rb.DEV_ACCEPT
     ptr = run.layer.pointers()
     assert list(ptr["h"]) == [w.T, 0] and (ptr["nd"] == 0).all()
+
+
+@pytest.mark.parametrize("T", [2, 4, 8])
+def test_gdn_draft_counts(T):
+    """GDN rounds in every draft bucket (3, 4 and 8), fp32 checkpoint."""
+    w = synth.WORKLOADS["gdn_spec"].with_(B=3, T=T, capacity=16 + T, precision="fp32", accept="uniform")
+    _run_spec(w, 10, seed=13)
