@@ -426,14 +426,30 @@ __device__ __forceinline__ void fold_store(const ReplayParams &p, const float (&
     }
 }
 
+// Ring position q of the stage ring: every consumer warp waits for every stage
+// in ring order and arrives once on each, after its last read; the producer
+// refills a stage only when all have.  A parity wait cannot tell a phase from
+// the one two phases later, so no warp may skip a stage or fall a ring behind.
+__device__ __forceinline__ bool wait_stage(uint64_t *full, int q, int NS, volatile int *abort_flag, uint32_t *status,
+                                           bool ok) {
+    ok = ok && wait_or_abort(full + q % NS, (unsigned)(q / NS) & 1u, abort_flag, status);
+    return __all_sync(0xffffffffu, ok);
+}
+__device__ __forceinline__ void release_stage(uint64_t *empty, int q, int NS) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(empty + q % NS);
+}
+
 // Fold of the lane's columns of a head whose NCB row blocks are all staged.
-// Coefficients are gathered fc records at a time.  fp32 blocks keep
-// the partial sums in place between chunks (each lane rewrites only its own
+// Coefficients are gathered fc records at a time.  fp32 blocks keep the
+// partial sums in place between chunks (each lane rewrites only its own
 // elements), so each chunk is gathered once per head; bf16 blocks (shared-bf16
-// checkpoints) keep them in registers, one row block at a time.
+// checkpoints) keep them in registers, one row block at a time.  Each row
+// block (ring position q0 + rb) is handed back as soon as its last read is
+// done, so the next copies overlap the rest of the fold.
 template <class C, typename TE>
 __device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages, int lane_off, int q0, int NS,
-                                          const uint16_t *kraw,
+                                          uint64_t *empty, const uint16_t *kraw,
                                           float *cfs, const FoldSrc &fs, const float *fw, float gf, int F, int j,
                                           int row0, int col0, int wcol0, int lcol, size_t goff, bool materialize,
                                           int lane, int fc) {
@@ -455,6 +471,12 @@ __device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages
 #pragma unroll
                         for (int e = 0; e < VEC; ++e) o[k][e] *= gf;
                 }
+                if (c == nch - 1) {
+                    // the block is in registers; partial sums written into the
+                    // stages by earlier chunks precede the copies this lets in
+                    if (nch > 1) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    release_stage(empty, q0 + rb, NS);
+                }
                 fold_records<C, TE>(o, kraw, cfs, lcol, r0, nr > 0 ? nr : 0, rb * RB + row0);
                 if (c == nch - 1) {
                     fold_store<C, TE>(p, o, rb * RB + row0, col0, goff, materialize);
@@ -465,8 +487,6 @@ __device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages
                 }
             }
         }
-        // the partial sums written into the stages precede the next copies into them
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     } else {
         for (int rb = 0; rb < NCB; ++rb) {
             float o[RK][VEC];
@@ -476,6 +496,7 @@ __device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) o[k][e] *= gf;
             }
+            release_stage(empty, q0 + rb, NS);  // the block is in registers
             for (int c = 0; c < nch; ++c) {
                 const int r0 = c * fc, nr = F - r0 < fc ? F - r0 : fc;
                 gather_fold_coefs<C>(cfs, fs, fw, r0, nr > 0 ? nr : 0, j, wcol0, lane);
@@ -484,20 +505,6 @@ __device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages
             fold_store<C, TE>(p, o, rb * RB + row0, col0, goff, materialize);
         }
     }
-}
-
-// Ring position q of the stage ring: every consumer warp waits for every stage
-// in ring order and arrives once on each, after its last read; the producer
-// refills a stage only when all have.  A parity wait cannot tell a phase from
-// the one two phases later, so no warp may skip a stage or fall a ring behind.
-__device__ __forceinline__ bool wait_stage(uint64_t *full, int q, int NS, volatile int *abort_flag, uint32_t *status,
-                                           bool ok) {
-    ok = ok && wait_or_abort(full + q % NS, (unsigned)(q / NS) & 1u, abort_flag, status);
-    return __all_sync(0xffffffffu, ok);
-}
-__device__ __forceinline__ void release_stage(uint64_t *empty, int q, int NS) {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(empty + q % NS);
 }
 
 // One pass of a warp over a head's row blocks (ring positions q0 ..
@@ -950,9 +957,8 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
         if (T == 0) {  // flush / materialise: fold only, the head's row blocks all resident
             for (int rb = 0; rb < NCB && ok; ++rb) ok = wait_stage(full, q0 + rb, NS, abort_flag, p.status, ok);
             if (!ok) break;
-            fold_head<C, TE>(p, const_cast<uint8_t *>(stages), lane_off, q0, NS, kraw, cfs, fs, fw, gF[j], F, j,
-                             row0, col0, wcol0, lcol, goff, materialize, lane, fc);
-            for (int rb = 0; rb < NCB; ++rb) release_stage(empty, q0 + rb, NS);
+            fold_head<C, TE>(p, const_cast<uint8_t *>(stages), lane_off, q0, NS, empty, kraw, cfs, fs, fw, gF[j], F,
+                             j, row0, col0, wcol0, lcol, goff, materialize, lane, fc);
             continue;
         }
         if (hold)
@@ -1043,9 +1049,10 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
         }
         if (hold) {
             if (keep)
-                fold_head<C, TE>(p, const_cast<uint8_t *>(stages), lane_off, q0, NS, kraw, cfs, fs, fw, gF[j], F, j,
-                                 row0, col0, wcol0, lcol, goff, materialize, lane, fc);
-            for (int rb = 0; rb < NCB; ++rb) release_stage(empty, q0 + rb, NS);
+                fold_head<C, TE>(p, const_cast<uint8_t *>(stages), lane_off, q0, NS, empty, kraw, cfs, fs, fw, gF[j],
+                                 F, j, row0, col0, wcol0, lcol, goff, materialize, lane, fc);
+            else
+                for (int rb = 0; rb < NCB; ++rb) release_stage(empty, q0 + rb, NS);
         }
     }
     it += HU * NCB;
