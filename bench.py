@@ -558,7 +558,7 @@ def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
     achieved = m["bytes_per_launch"] / (m["launch_ms"] * 1e-3) / 1e9
     clk = ClockSampler.summarise(m["clock_rows"], *m["t_wall"]) if m["clock_rows"] else None
     kernel = {"mamba2": "rows::replay_pipe_kernel<mamba2, P=64, N=128, HU=8, TMAX=1, NC=256, NS=2, SPLIT=1>",
-              "gdn": "cols::replay_pipe_kernel<gdn, P=128, N=128, TMAX=1> (launch: HU=2, NS=4, 2 CTAs/SM)"}[w.kind]
+              "gdn": "cols::replay_pipe_kernel<gdn, P=128, N=128, TMAX=1, TC=0> (launch: HU=2, NS=5, 2 CTAs/SM)"}[w.kind]
     out = {
         "metric": METRIC,
         "value": w.B * K * world / (ms_total * 1e-3),

@@ -49,7 +49,7 @@ std::mutex g_limits_mu;
 
 }  // namespace
 
-bool encode_slab_map(CUtensorMap *map, const void *base, bool bf16, int P, int N, long long slabs) {
+bool encode_slab_map(CUtensorMap *map, const void *base, bool bf16, int P, int N, long long slabs, bool col_blocks) {
     const EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t esz = bf16 ? 2 : 4, cb = 128 / esz;
@@ -58,8 +58,10 @@ bool encode_slab_map(CUtensorMap *map, const void *base, bool bf16, int P, int N
     const cuuint64_t strides[3] = {128, (cuuint64_t)P * esz, (cuuint64_t)N * P * esz};  // bytes, dims 1..3
     const cuuint64_t lines = (cuuint64_t)P / cb;  // 128-byte lines per row
     if (N % lines != 0 || N / lines > 256) return false;
-    // one box = one row block: N / lines whole rows, i.e. N x 128 bytes
-    const cuuint32_t box[4] = {(cuuint32_t)cb, (cuuint32_t)lines, (cuuint32_t)(N / lines), 1};
+    // one box = one row block: N / lines whole rows, i.e. N x 128 bytes; or
+    // (col_blocks) one column block: the same 128-byte line of all N rows
+    const cuuint32_t box[4] = {(cuuint32_t)cb, col_blocks ? 1u : (cuuint32_t)lines,
+                               col_blocks ? (cuuint32_t)N : (cuuint32_t)(N / lines), 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

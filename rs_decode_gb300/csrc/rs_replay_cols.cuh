@@ -74,6 +74,15 @@ struct RCfg {
     // the Mamba-2 output reduction halves down to single sums: a power-of-two bucket
     static_assert(KIND == RS_GDN || (JP & (JP - 1)) == 0, "draft bucket");
     static constexpr int JPP = JP <= 1 ? 1 : 2 << ilog2(JP - 1);  // JP rounded up to a power of two
+    // bf16 row blocks of GDN heads (P = 128: both blocks of a head form one
+    // M = 128 operand) are dotted on the tensor cores: D[P x 16] = S_c^T-view x
+    // [the JP dot vectors, zero padded], in TMEM
+    static constexpr bool UMMA = KIND == RS_GDN && P == 128 && N % 16 == 0 && JP <= 16;
+    static constexpr int UMMA_N = 16;                     // MMA N (vectors, padded)
+    static constexpr int UMMA_TCOLS = 32;                 // TMEM columns: two D buffers
+    // the B operand: bf16 vectors as K-major 8 x 8 core matrices, one group of
+    // 8 vectors (two when JP > 8); a unit uses it instead of the fp32 vectors
+    static constexpr int QB_BYTES = (JP > 8 ? 2 : 1) * N * 16;
 };
 
 // Where a consumer warp's lanes sit in a stage of element type TE.  A row of
@@ -131,7 +140,7 @@ struct UnitHdr {
 // consumer warps' scratch (fcf: fw_r v_r for the warp's P/NCW columns, for
 // fold_chunk(cap) records at a time).
 struct RSmem {
-    int stages, bars, plans, abort, d1, d2, sr, cst, fcf, ctx0, ctx_bytes;
+    int stages, bars, plans, abort, tmem, d1, d2, sr, cst, fcf, ctx0, ctx_bytes;
     int hdr, kraw, ar, vb, bt, c1, c2, g1, g2, fw, gF, pre1, pre2, qs, unew;  // within a context
     int total;
 };
@@ -151,9 +160,10 @@ __host__ __device__ inline RSmem replay_smem(int cap, int HU, int NS) {
     RSmem s;
     int o = 0;
     s.stages = o; o += NS * C::STAGE;
-    s.bars = o;   o += al16((2 * NS + 6 + 2 * kPlanRing) * 8);      // stage, context and plan barriers
+    s.bars = o;   o += al16((2 * NS + 6 + 2 * kPlanRing + 4) * 8);  // stage, context, plan, MMA barriers
     s.plans = o;  o += al16(kPlanRing * (int)sizeof(UnitHdr));
     s.abort = o;  o += 16;
+    s.tmem = o;   o += 16;                                          // TMEM address of the D buffers
     s.d1 = o;     o += al16(cap * TMAX * 4);                        // k_r . q_i (GDN: k_r . k_{m_i})
     s.d2 = o;     o += GDN ? al16(cap * TMAX * 4) : 0;              // GDN k_r . q_i
     s.sr = o;     o += al16(HU * cap * 4);                          // Mamba-2 dt_r
@@ -173,13 +183,41 @@ __host__ __device__ inline RSmem replay_smem(int cap, int HU, int NS) {
     s.gF = c;     c += al16(HU * 4);
     s.pre1 = c;   c += al16(HU * TMAX * P * 4);                     // record parts of the outputs
     s.pre2 = c;   c += GDN ? al16(HU * TMAX * P * 4) : 0;
-    s.qs = c;     c += al16(N * C::JP * 4);                         // fp32 dot vectors, [QC][N][QW]
+    // fp32 dot vectors [QC][N][QW], or (tensor-core units) the bf16 B operand
+    s.qs = c;     c += al16(C::UMMA && C::QB_BYTES > N * C::JP * 4 ? C::QB_BYTES : N * C::JP * 4);
     s.unew = c;   c += GDN ? al16(HU * TMAX * P * 4) : 0;           // GDN: u of this launch's records
     s.ctx_bytes = c;
     s.ctx0 = o;   o += 2 * c;
     s.total = o;
     return s;
 }
+
+// Whether a launch dots its bf16 blocks on the tensor cores: two-precision
+// checkpoints (bf16 reads never fold, so nothing but the MMAs reads a bf16
+// stage).  The ring depth is then even, so that the two blocks of a head (ring
+// positions q0, q0 + 1 with q0 even) are adjacent stages, and the bf16 copy is
+// streamed in column blocks: a stage holds one 64-column half of the slab for
+// all N keys, line n = key n, the layout of an MN-major operand.
+template <class C>
+__host__ __device__ inline bool umma_prec(const ReplayParams &p) {
+    return C::UMMA && p.prec == RS_PREC_TWO && p.ckpt_lp != nullptr;
+}
+
+// Shared memory of one pipeline: its carve-up, rounded to the 1024-byte
+// alignment of the next pipeline's stages.
+__host__ __device__ inline int pipe_bytes(const RSmem &L) { return (L.total + 1023) & ~1023; }
+
+// Where a pipeline sits in its CTA.  A CTA runs one pipeline (NT threads), or
+// two side by side (2 NT threads, two carve-ups): kernels that hold tensor
+// memory are resident one CTA per SM, so they pair their pipelines in one CTA.
+struct PipeCtx {
+    int u0, ustride;        // the pipeline's units: u0, u0 + ustride, ...
+    int tid;                // thread index within the pipeline
+    int bar_prep;           // named barrier of the pipeline's prep warps
+    bool tc;                // bf16 blocks are dotted on the tensor cores
+    const uint32_t *tslot;  // TMEM address of the CTA's allocation
+    uint32_t tcol;          // the pipeline's first TMEM column
+};
 
 // VEC consecutive bf16 values (VEC = 4: 8-byte aligned, VEC = 8: 16-byte aligned) as fp32.
 template <int VEC>
@@ -284,18 +322,23 @@ __device__ __forceinline__ void reduce_rows(float (&acc)[WGeo<C, TE>::M], int rg
 // Planner (one lane of the producer warp): reads each unit's pointers, takes
 // part in the pointer update, and hands the plan to the prep warps through a
 // ring of kPlanRing slots, so that the pointer reads and the arrival atomic of
-// later units overlap the prep warps' work on the current one.
+// later units overlap the prep warps' work on the current one.  A plan with
+// b = -1 ends the pipeline.
 template <class C>
 __device__ __forceinline__ void planner(const ReplayParams &p, uint8_t *sm, const RSmem &L, int units, int HU,
-                                        int NS) {
+                                        int NS, const PipeCtx &pc) {
     uint64_t *pfull = reinterpret_cast<uint64_t *>(sm + L.bars) + 2 * NS + 6, *pempty = pfull + kPlanRing;
     UnitHdr *plans = reinterpret_cast<UnitHdr *>(sm + L.plans);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
     const unsigned upseq = p.H / HU;
-    int cu = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++cu) {
+    for (int cu = 0, u = pc.u0;; ++cu, u += pc.ustride) {
         const int slot = cu % kPlanRing;
         if (!wait_or_abort(pempty + slot, ((cu / kPlanRing) & 1) ^ 1, abort_flag, p.status)) return;
+        if (u >= units) {
+            plans[slot].b = -1;
+            mbar_arrive(pfull + slot);
+            return;
+        }
         const int b = u / upseq;
         const SeqPlan s = plan_sequence(p, b);
         arrive_and_update(p, s, b, upseq, (u % upseq) == 0);
@@ -310,29 +353,32 @@ __device__ __forceinline__ void planner(const ReplayParams &p, uint8_t *sm, cons
 // Producer: stream each unit's row blocks once the prep warps have planned it.
 template <class C>
 __device__ __forceinline__ void producer(const ReplayParams &p, uint8_t *sm, const RSmem &L, int units, int HU,
-                                         int NS, const CUtensorMap *map_hp, const CUtensorMap *map_lp) {
+                                         int NS, const CUtensorMap *map_hp, const CUtensorMap *map_lp,
+                                         const PipeCtx &pc) {
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + L.bars), *empty = full + NS, *cplan = empty + NS;
     uint64_t *cempty = cplan + 4;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
     int st = 0, ph = 0, issued = 0, cu = 0;
     bool stop = false;
-    for (int u = blockIdx.x; u < units && !stop; u += gridDim.x, ++cu) {
+    for (; !stop; ++cu) {
         const int buf = cu & 1;
         if (!wait_or_abort(cplan + buf, (cu >> 1) & 1, abort_flag, p.status)) break;
         const UnitHdr hd = *reinterpret_cast<const UnitHdr *>(sm + L.ctx0 + buf * L.ctx_bytes + L.hdr);
+        if (hd.b < 0) break;  // the pipeline's last unit is streamed
         // the prep warps rebuild this context only after this arrival (and the
         // consumer warps'), so no plan phase can pass unread
         mbar_arrive(cempty + buf);
         if (!hd.s.work) continue;
         const bool lp = plan_reads_lp(p, hd.s);
+        const bool colb = lp && pc.tc;  // bf16 column blocks for the tensor cores
         const CUtensorMap *map = lp ? map_lp : map_hp;
         const int ncb = C::P * (lp ? 2 : 4) / 128, rb_rows = C::N / ncb;
         for (int j = 0; j < HU && !stop; ++j) {
             for (int rb = 0; rb < ncb; ++rb) {
                 if (!wait_or_abort(empty + st, ph ^ 1, abort_flag, p.status)) { stop = true; break; }
                 mbar_arrive_expect_tx(full + st, C::STAGE);
-                tma_load_4d(sm + L.stages + (size_t)st * C::STAGE, map, 0, 0, rb * rb_rows, hd.b * p.H + hd.h0 + j,
-                            full + st);
+                tma_load_4d(sm + L.stages + (size_t)st * C::STAGE, map, 0, colb ? rb : 0, colb ? 0 : rb * rb_rows,
+                            hd.b * p.H + hd.h0 + j, full + st);
                 ++issued;
                 if (++st == NS) { st = 0; ph ^= 1; }
             }
@@ -534,9 +580,10 @@ __device__ __forceinline__ bool head_pass(float (&acc)[WGeo<C, TE>::M], const Re
 // in the context buffer `cx`.  Returns false when the CTA aborts.
 template <class C>
 __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, const RSmem &L, uint8_t *cx,
-                                          const SeqPlan &s, const int b, const int h0, const int HU) {
+                                          const SeqPlan &s, const int b, const int h0, const int HU, const bool tcu,
+                                          const PipeCtx &pc) {
     constexpr int KIND = C::KIND, P = C::P, N = C::N, TMAX = C::TMAX, NPT = C::NPT, JP = C::JP;
-    const int tp = threadIdx.x - C::PREP0, lane = tp & 31, pw = tp >> 5;
+    const int tp = pc.tid - C::PREP0, lane = tp & 31, pw = tp >> 5;
     const int H = p.H, G = p.G, cap = p.cap;
     const int g = h0 / (H / G);
     const int base = s.base, hc = s.hc, T = s.T, F = s.F;
@@ -630,7 +677,7 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
         }
         cp_async_wait_all();
     }
-    if (named_sync_or(1, NPT, false)) return false;
+    if (named_sync_or(pc.bar_prep, NPT, false)) return false;
 
     // ---- 2. new records' decays; appends; the fp32 dot vectors
     for (int i2 = tp; i2 < HU * T; i2 += NPT) {
@@ -665,7 +712,21 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
         if (jj < TMAX) return jj < T ? hc + jj : -1;
         return jj - TMAX < T ? cap + jj - TMAX : -1;
     };
-    if (T > 0) {
+    if (C::UMMA && T > 0 && tcu) {
+        // the tensor cores' B operand (bf16): slot jj's keys 8c .. 8c+7 form
+        // row jj % 8 of core matrix (jj / 8, c), core matrices 128 bytes apart
+        // along the keys and N*16 bytes apart across groups of 8 slots; slots
+        // past the launch's vectors are zero
+        constexpr int KC = N / 8, NB = C::QB_BYTES / (N * 2);
+        uint8_t *qb = reinterpret_cast<uint8_t *>(qs);
+        for (int i2 = tp; i2 < NB * KC; i2 += NPT) {
+            const int jj = i2 / KC, c = i2 % KC;
+            const int row = jj < JP ? slot_row(jj) : -1;
+            const uint4 v = row >= 0 ? ld_u4(kraw + (size_t)row * N + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4 *>(qb + (jj / 8) * (KC * 128) + c * 128 + (jj % 8) * 16) = v;
+        }
+        fence_proxy_async_smem();  // read by the tensor cores (async proxy)
+    } else if (T > 0) {
         // one key row n per task: its JP slots as fp32, QW at a time
         for (int n = tp; n < N; n += NPT) {
 #pragma unroll
@@ -729,7 +790,7 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
             }
         }
     }
-    if (named_sync_or(1, NPT, false)) return false;
+    if (named_sync_or(pc.bar_prep, NPT, false)) return false;
 
     // ---- 4. decay coefficients per head
     // Record positions are 0-based; draft i sits at m_i = hc + i.  With
@@ -782,7 +843,7 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
         }
         if (F == 0 && lane == 0) gF[hd] = 1.f;
     }
-    if (named_sync_or(1, NPT, false)) return false;
+    if (named_sync_or(pc.bar_prep, NPT, false)) return false;
 
     // ---- 5. the parts of the outputs that come from the records, per value column
     if (KIND == RS_MAMBA2 && T > 0) {
@@ -832,7 +893,7 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
                 }
             }
         }
-        if (named_sync_or(1, NPT, false)) return false;
+        if (named_sync_or(pc.bar_prep, NPT, false)) return false;
     }
     // GDN: committed-record parts of S_{m_i-1} k_{m_i} and S_{m_i} q_i: one
     // task per head and 4 columns, all drafts at once; the committed u come
@@ -881,7 +942,7 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
                 }
             }
         }
-        if (named_sync_or(1, NPT, false)) return false;
+        if (named_sync_or(pc.bar_prep, NPT, false)) return false;
     }
     return true;
 }
@@ -890,16 +951,16 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
 // Consumer warps: the heads of one unit from its context `cx`, each warp on
 // its own value columns.  `it` is the ring position of the unit's first
 // stage.  Returns false when the CTA aborts.
-template <class C, typename TE>
+template <class C, bool TC, typename TE>
 __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm, const RSmem &L, const uint8_t *cx,
                                               const SeqPlan &s, const int b, const int h0, const int HU,
-                                              const int NS, int &it) {
+                                              const int NS, int &it, const PipeCtx &pc, int &mseq, bool &inflight) {
     constexpr int KIND = C::KIND, P = C::P, N = C::N, TMAX = C::TMAX, JP = C::JP;
     using W = WGeo<C, TE>;
     constexpr int VEC = W::VEC, RGW = W::RGW, LR = W::LR, M = W::M, NCB = W::NCB, JN = W::JN, NPASS = W::NPASS;
     constexpr int RB = W::RB;
     static_assert(NPASS == 1 || NPASS == 2 || (NPASS == 4 && KIND == RS_GDN), "passes");
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lane = pc.tid & 31, warp = pc.tid >> 5;
     const int H = p.H, cap = p.cap, mode = p.mode;
     const int base = s.base, hc = s.hc, T = s.T, F = s.F;
     const bool append = s.append, materialize = mode == MODE_MATERIALIZE;
@@ -907,6 +968,7 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
     auto slot = [&](int r) { return (base + r) % cap; };
 
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + L.bars), *empty = full + NS;
+    uint64_t *mdone = full + 2 * NS + 6 + 2 * kPlanRing, *dfree = mdone + 2;  // tensor-core D buffers
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
     const uint16_t *kraw = reinterpret_cast<const uint16_t *>(cx + L.kraw);
     float *unew = const_cast<float *>(reinterpret_cast<const float *>(cx + L.unew));  // GDN: u of new records
@@ -992,33 +1054,84 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
                 outputs(JN);
             }
         } else {
-            // GDN: per value column, the recurrence over the drafts.  The
-            // reductions keep all sums of one column in one lane: slots i < TMAX
-            // hold (S_c k_{m_i})[p], slots TMAX + i hold (S_c q_i)[p].
-            constexpr int HV = ilog2(VEC);
-            const int e = rg >> (LR - HV), pp = col0 + e;
-            const bool lead = (rg & ((1 << (LR - HV)) - 1)) == 0;
+            // GDN: per value column, the recurrence over the drafts.  sums[jj]
+            // holds (S_c v_jj)[pp] of the lane's column pp: slots i < TMAX the
+            // keys k_{m_i}, slots TMAX + i the queries q_i.
             float sums[JP];
-            ok = head_pass<C, TE, 0>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qs, row0, hold);
-            if (!ok) break;
-            reduce_rows<C, TE, JN>(acc, rg);
+            int pp;
+            bool lead;
+            if constexpr (TC && C::UMMA && sizeof(TE) == 2) {
+                // Tensor cores: D[p][jj] = sum_n S_c[n][p] v_jj[n] for the head's
+                // two row blocks (M = 128 value columns, K = N keys, A read from
+                // the staged 128-byte-swizzled lines as an MN-major operand, B the
+                // unit's bf16 vectors).  Warp 0 issues after the copies landed and
+                // the D buffer's previous readers are done; every warp then reads
+                // its 32 columns.  Double-buffered D: mseq counts the MMA heads.
+                constexpr int NLD = JP <= 2 ? 2 : JP <= 4 ? 4 : JP <= 8 ? 8 : 16;
+                const int db = mseq & 1;
+                const unsigned use = (unsigned)mseq >> 1;
+                const uint32_t tbase = *reinterpret_cast<const volatile uint32_t *>(pc.tslot) + pc.tcol;
+                if (warp == 0) {
+                    if (!hold)
+                        for (int rb = 0; rb < NCB && ok; ++rb) ok = wait_stage(full, q0 + rb, NS, abort_flag, p.status, ok);
+                    if (ok && use > 0)
+                        ok = __all_sync(0xffffffffu, wait_or_abort(dfree + db, (use - 1) & 1u, abort_flag, p.status));
+                    if (ok && lane == 0) {
+                        tc_fence_after_sync();
+                        const uint32_t a0 = smem_u32(stages + (size_t)(q0 % NS) * C::STAGE), b0 = smem_u32(qs);
+                        constexpr uint32_t idesc = umma_idesc_bf16(128, C::UMMA_N, true, false);
 #pragma unroll
-            for (int t = 0; t < JN; ++t) sums[t] = acc[t];
-            if constexpr (NPASS >= 2) {
-                head_pass<C, TE, JN>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qs, row0, hold);
+                        for (int ks = 0; ks < N / 16; ++ks)
+                            umma_bf16(tbase + db * C::UMMA_N, umma_smem_desc(a0 + ks * 2048, C::STAGE, 1024, 2),
+                                      umma_smem_desc(b0 + ks * 256, 128, JP > 8 ? N * 16 : 0, 0), idesc, ks > 0);
+                        umma_commit(mdone + db);
+                    }
+                    inflight = ok;
+                    __syncwarp();
+                }
+                ok = ok && __all_sync(0xffffffffu, wait_or_abort(mdone + db, use & 1u, abort_flag, p.status));
+                if (!ok) break;
+                if (warp == 0) inflight = false;
+                tc_fence_after_sync();
+                float dv[NLD];
+                tmem_ld<NLD>(tbase + ((uint32_t)(32 * warp) << 16) + db * C::UMMA_N, dv);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(dfree + db);  // this warp has read the D buffer
+                if (!hold)  // the MMAs have read the row blocks
+                    for (int rb = 0; rb < NCB; ++rb) release_stage(empty, q0 + rb, NS);
+                ++mseq;
+#pragma unroll
+                for (int t = 0; t < JP; ++t) sums[t] = dv[t];
+                pp = 32 * warp + lane;
+                lead = true;
+            } else {
+                // CUDA cores: the reductions keep all sums of one column in one lane
+                constexpr int HV = ilog2(VEC);
+                const int e = rg >> (LR - HV);
+                pp = col0 + e;
+                lead = (rg & ((1 << (LR - HV)) - 1)) == 0;
+                ok = head_pass<C, TE, 0>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qs, row0, hold);
+                if (!ok) break;
                 reduce_rows<C, TE, JN>(acc, rg);
 #pragma unroll
-                for (int t = 0; t < JN; ++t) sums[JN + t] = acc[t];
-            }
-            if constexpr (NPASS == 4) {
-                head_pass<C, TE, 2 * JN>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qs, row0, hold);
-                reduce_rows<C, TE, JN>(acc, rg);
+                for (int t = 0; t < JN; ++t) sums[t] = acc[t];
+                if constexpr (NPASS >= 2) {
+                    head_pass<C, TE, JN>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qs, row0, hold);
+                    reduce_rows<C, TE, JN>(acc, rg);
 #pragma unroll
-                for (int t = 0; t < JN; ++t) sums[2 * JN + t] = acc[t];
-                head_pass<C, TE, 3 * JN>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qs, row0, hold);
-                reduce_rows<C, TE, JN>(acc, rg);
+                    for (int t = 0; t < JN; ++t) sums[JN + t] = acc[t];
+                }
+                if constexpr (NPASS == 4) {
+                    head_pass<C, TE, 2 * JN>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qs, row0, hold);
+                    reduce_rows<C, TE, JN>(acc, rg);
 #pragma unroll
-                for (int t = 0; t < JN; ++t) sums[3 * JN + t] = acc[t];
+                    for (int t = 0; t < JN; ++t) sums[2 * JN + t] = acc[t];
+                    head_pass<C, TE, 3 * JN>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qs, row0, hold);
+                    reduce_rows<C, TE, JN>(acc, rg);
+#pragma unroll
+                    for (int t = 0; t < JN; ++t) sums[3 * JN + t] = acc[t];
+                }
             }
             float ud[TMAX];
 #pragma unroll
@@ -1063,22 +1176,19 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
 // Role loops.
 template <class C>
 __device__ __forceinline__ void prep_loop(const ReplayParams &p, uint8_t *sm, const RSmem &L, int units, int HU,
-                                          int NS) {
+                                          int NS, const PipeCtx &pc) {
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bars);
     uint64_t *cplan = bars + 2 * NS, *cfull = cplan + 2, *cempty = cfull + 2;
     uint64_t *pfull = cempty + 2, *pempty = pfull + kPlanRing;
     const UnitHdr *plans = reinterpret_cast<const UnitHdr *>(sm + L.plans);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
-    const unsigned upseq = p.H / HU;
-    const int tp = threadIdx.x - C::PREP0;
-    int cu = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++cu) {
+    const int tp = pc.tid - C::PREP0;
+    for (int cu = 0;; ++cu) {
         const int buf = cu & 1;
         const bool ok = wait_or_abort(cempty + buf, ((cu >> 1) & 1) ^ 1, abort_flag, p.status);
-        if (named_sync_or(1, C::NPT, !ok)) return;  // the producer and every consumer warp are done with it
+        if (named_sync_or(pc.bar_prep, C::NPT, !ok)) return;  // the producer and every consumer warp are done with it
         uint8_t *cx = sm + L.ctx0 + buf * L.ctx_bytes;
         UnitHdr *hdr = reinterpret_cast<UnitHdr *>(cx + L.hdr);
-        const int b = u / upseq, h0 = (u % upseq) * HU;
         if (tp == 0) {
             // the unit's plan, from the planner lane
             const int slot = cu % kPlanRing;
@@ -1089,32 +1199,40 @@ __device__ __forceinline__ void prep_loop(const ReplayParams &p, uint8_t *sm, co
                 mbar_arrive(cplan + buf);  // release: the producer may stream the unit
             }
         }
-        if (named_sync_or(1, C::NPT, *abort_flag != 0)) return;
+        if (named_sync_or(pc.bar_prep, C::NPT, *abort_flag != 0)) return;
+        const int b = hdr->b, h0 = hdr->h0;
+        if (b < 0) {  // no more units: the consumer warps see the end plan too
+            if (tp == 0) mbar_arrive(cfull + buf);
+            return;
+        }
         const SeqPlan s = hdr->s;
-        if (s.work && !prep_unit<C>(p, sm, L, cx, s, b, h0, HU)) return;
-        if (named_sync_or(1, C::NPT, false)) return;  // the whole context is written
+        if (s.work && !prep_unit<C>(p, sm, L, cx, s, b, h0, HU, pc.tc && plan_reads_lp(p, s), pc)) return;
+        if (named_sync_or(pc.bar_prep, C::NPT, false)) return;  // the whole context is written
         if (tp == 0) mbar_arrive(cfull + buf);
     }
 }
 
-template <class C>
+template <class C, bool TC>
 __device__ __forceinline__ void consumer_loop(const ReplayParams &p, uint8_t *sm, const RSmem &L, int units, int HU,
-                                              int NS) {
+                                              int NS, const PipeCtx &pc, int &mseq, bool &inflight) {
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bars);
     uint64_t *cfull = bars + 2 * NS + 2, *cempty = cfull + 2;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
-    const int lane = threadIdx.x & 31;
-    int it = 0, cu = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++cu) {
+    const int lane = pc.tid & 31;
+    int it = 0;
+    for (int cu = 0;; ++cu) {
         const int buf = cu & 1;
         const bool ok = __all_sync(0xffffffffu, wait_or_abort(cfull + buf, (cu >> 1) & 1, abort_flag, p.status));
         if (!ok) return;
         const uint8_t *cx = sm + L.ctx0 + buf * L.ctx_bytes;
         const UnitHdr hd = *reinterpret_cast<const UnitHdr *>(cx + L.hdr);
+        if (hd.b < 0) return;
         if (hd.s.work) {
             const bool done = plan_reads_lp(p, hd.s)
-                                  ? consume_heads<C, uint16_t>(p, sm, L, cx, hd.s, hd.b, hd.h0, HU, NS, it)
-                                  : consume_heads<C, float>(p, sm, L, cx, hd.s, hd.b, hd.h0, HU, NS, it);
+                                  ? consume_heads<C, TC, uint16_t>(p, sm, L, cx, hd.s, hd.b, hd.h0, HU, NS, it, pc,
+                                                                   mseq, inflight)
+                                  : consume_heads<C, TC, float>(p, sm, L, cx, hd.s, hd.b, hd.h0, HU, NS, it, pc, mseq,
+                                                                inflight);
             if (!done) return;
         }
         __syncwarp();
@@ -1122,15 +1240,28 @@ __device__ __forceinline__ void consumer_loop(const ReplayParams &p, uint8_t *sm
     }
 }
 
-template <class C>
-__global__ void __launch_bounds__(C::NT, C::MIN_BLOCKS)
+// TC: the kernel holds tensor memory (the bf16 blocks of two-precision
+// launches are dotted on the tensor cores); such kernels are resident one CTA
+// per SM, so they run PIPES = 2 pipelines side by side in one CTA.
+template <class C, bool TC, int PIPES>
+__global__ void __launch_bounds__(C::NT * PIPES, PIPES == 1 ? C::MIN_BLOCKS : 1)
     replay_pipe_kernel(const ReplayParams p, const __grid_constant__ CUtensorMap map_hp,
                        const __grid_constant__ CUtensorMap map_lp, int units, int HU, int NS) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the swizzle pattern is a function of the shared address: align the carve-up to 1024 bytes
-    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *sm0 = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const RSmem L = replay_smem<C>(p.cap, HU, NS);
-    if (threadIdx.x == 0) {
+    const int pipe = PIPES == 1 ? 0 : (int)(threadIdx.x / C::NT);
+    uint8_t *sm = sm0 + (size_t)pipe * pipe_bytes(L);
+    PipeCtx pc;
+    pc.u0 = blockIdx.x * PIPES + pipe;
+    pc.ustride = gridDim.x * PIPES;
+    pc.tid = threadIdx.x & (C::NT - 1);
+    pc.bar_prep = 1 + pipe;  // named barriers 1 .. PIPES; PIPES + 1: every consumer warp of the CTA
+    pc.tc = TC;
+    pc.tslot = reinterpret_cast<const uint32_t *>(sm0 + L.tmem);
+    pc.tcol = (uint32_t)(pipe * C::UMMA_TCOLS);
+    if (pc.tid == 0) {
         uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bars);
         for (int s = 0; s < NS; ++s) {
             mbar_init(bars + s, 1);             // full: the producer's expect_tx arrival
@@ -1146,18 +1277,43 @@ __global__ void __launch_bounds__(C::NT, C::MIN_BLOCKS)
             mbar_init(pb + 6 + k, 1);               // plan full: the planner lane
             mbar_init(pb + 6 + kPlanRing + k, 1);   // plan empty: the prep warps
         }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(pb + 6 + 2 * kPlanRing + k, 1);       // MMA done: the issuing thread's commit
+            mbar_init(pb + 8 + 2 * kPlanRing + k, C::NCW);  // D buffer read: every consumer warp
+        }
         *reinterpret_cast<volatile int *>(sm + L.abort) = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    const int warp = pc.tid >> 5;
+    if constexpr (TC) {
+        if (threadIdx.x < 32) tmem_alloc(reinterpret_cast<uint32_t *>(sm0 + L.tmem), C::UMMA_TCOLS * PIPES);
+        tc_fence_before_sync();
+    }
     __syncthreads();
-    const int warp = threadIdx.x >> 5;
+    if constexpr (TC) tc_fence_after_sync();
     if (warp < C::NCW) {
-        consumer_loop<C>(p, sm, L, units, HU, NS);
+        int mseq = 0;
+        bool inflight = false;
+        consumer_loop<C, TC>(p, sm, L, units, HU, NS, pc, mseq, inflight);
+        if constexpr (TC) {
+            // the TMEM goes back once no MMA is in flight and every consumer
+            // warp of the CTA is done with it (also after an abort)
+            if (warp == 0 && inflight) {
+                uint64_t *mdone = reinterpret_cast<uint64_t *>(sm + L.bars) + 2 * NS + 6 + 2 * kPlanRing;
+                mbar_wait(mdone + (mseq & 1), ((unsigned)mseq >> 1) & 1u);
+            }
+            tc_fence_before_sync();
+            asm volatile("bar.sync %0, %1;" ::"n"(PIPES + 1), "n"(32 * C::NCW * PIPES) : "memory");
+            if (threadIdx.x < 32) {
+                tc_fence_after_sync();
+                tmem_dealloc(*reinterpret_cast<const volatile uint32_t *>(pc.tslot), C::UMMA_TCOLS * PIPES);
+            }
+        }
     } else if (warp == C::NCW) {
-        if (threadIdx.x == 32 * C::NCW) producer<C>(p, sm, L, units, HU, NS, &map_hp, &map_lp);
-        else if (threadIdx.x == 32 * C::NCW + 1) planner<C>(p, sm, L, units, HU, NS);
+        if (pc.tid == 32 * C::NCW) producer<C>(p, sm, L, units, HU, NS, &map_hp, &map_lp, pc);
+        else if (pc.tid == 32 * C::NCW + 1) planner<C>(p, sm, L, units, HU, NS, pc);
     } else {
-        prep_loop<C>(p, sm, L, units, HU, NS);
+        prep_loop<C>(p, sm, L, units, HU, NS, pc);
     }
 }
 
@@ -1168,9 +1324,10 @@ __global__ void __launch_bounds__(C::NT, C::MIN_BLOCKS)
 // elements = 128 bytes innermost; the box is one row block of one slab
 // (CB x P/CB x N*CB/P x 1: contiguous in HBM, N x 128 bytes), landing in shared
 // memory as 128-byte lines with the 128-byte swizzle.
-bool encode_slab_map(CUtensorMap *map, const void *base, bool bf16, int P, int N, long long slabs);
+bool encode_slab_map(CUtensorMap *map, const void *base, bool bf16, int P, int N, long long slabs, bool col_blocks);
 
-// Launch shape: heads per unit, ring depth, CTAs per SM, shared memory.
+// Launch shape: heads per unit, ring depth, CTAs per SM (pipelines per CTA
+// for tensor-core kernels), shared memory.
 struct LaunchShape {
     int HU, NS, per_sm, smem;
 };
@@ -1181,13 +1338,14 @@ struct DeviceLimits {
 };
 cudaError_t device_limits(DeviceLimits &d);
 
+// CUDA-core kernels: two CTAs per SM (one CTA's per-unit phases overlap the
+// other's stream), at least four stages each; else one CTA per SM with a
+// deeper ring.
 template <class C>
 LaunchShape choose_shape(const ReplayParams &p, const DeviceLimits &dl) {
     const int hpg = p.H / p.G;
     static constexpr int kHU[] = {8, 4, 2, 1};
     LaunchShape best = {0, 0, 0, 0};
-    // two CTAs per SM (one CTA's per-unit phases overlap the other's stream),
-    // at least four stages each; else one CTA per SM with a deeper ring
     for (int tier = C::MIN_BLOCKS == 2 ? 2 : 1; tier >= 1 && best.HU == 0; --tier) {
         const int budget = (tier == 2 ? dl.smem_per_sm / 2 - dl.reserved_per_block : dl.smem_per_block) - 1024;
         // a held head keeps all its row blocks resident: at least one fp32 slab of stages
@@ -1211,34 +1369,77 @@ LaunchShape choose_shape(const ReplayParams &p, const DeviceLimits &dl) {
     return best;
 }
 
+// Tensor-core kernels (one CTA per SM): two pipelines per CTA, each with half
+// of the CTA's shared memory, at least four stages each; else one pipeline
+// with a deeper ring.  The ring depth is even (a head's two bf16 blocks are
+// adjacent stages).  per_sm holds the pipelines per CTA.
 template <class C>
-cudaError_t launch_pipe(const ReplayParams &p, cudaStream_t stream) {
-    DeviceLimits dl;
-    cudaError_t e = device_limits(dl);
-    if (e != cudaSuccess) return e;
-    const LaunchShape sh = choose_shape<C>(p, dl);
-    if (sh.HU == 0) return cudaErrorInvalidConfiguration;
-    auto kern = replay_pipe_kernel<C>;
+LaunchShape choose_shape_tc(const ReplayParams &p, const DeviceLimits &dl) {
+    const int hpg = p.H / p.G;
+    static constexpr int kHU[] = {8, 4, 2, 1};
+    for (int pipes = 2; pipes >= 1; --pipes) {
+        const int budget = pipes == 2 ? ((dl.smem_per_block - 1024) / 2) & ~1023 : dl.smem_per_block - 1024;
+        const int ns_max = pipes == 2 ? 8 : 12, ns_min = C::P * 4 / 128 > 4 ? C::P * 4 / 128 : 4;
+        for (int HU : kHU) {
+            if (hpg % HU != 0) continue;
+            const int other = replay_smem<C>(p.cap, HU, 0).total;
+            int ns = (budget - other) / C::STAGE;
+            if (ns > ns_max) ns = ns_max;
+            ns &= ~1;
+            if (ns < ns_min) continue;
+            const RSmem L = replay_smem<C>(p.cap, HU, ns);
+            return {HU, ns, pipes, (pipes == 2 ? 2 * pipe_bytes(L) : L.total) + 1024};
+        }
+    }
+    return {0, 0, 0, 0};
+}
+
+template <class C, bool TC, int PIPES>
+cudaError_t launch_kernel(const ReplayParams &p, const LaunchShape &sh, const DeviceLimits &dl,
+                          cudaStream_t stream) {
+    auto kern = replay_pipe_kernel<C, TC, PIPES>;
     static bool attr_set = false;
+    cudaError_t e;
     if (!attr_set) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dl.smem_per_block);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::NT, sh.smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::NT * PIPES, sh.smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     CUtensorMap map_hp, map_lp;
     memset(&map_hp, 0, sizeof map_hp);
     memset(&map_lp, 0, sizeof map_lp);
     const long long slabs = (long long)p.B * p.H;
-    if (p.ckpt_hp && !encode_slab_map(&map_hp, p.ckpt_hp, false, C::P, C::N, slabs)) return cudaErrorInvalidValue;
-    if (p.ckpt_lp && !encode_slab_map(&map_lp, p.ckpt_lp, true, C::P, C::N, slabs)) return cudaErrorInvalidValue;
-    const int units = p.B * (p.H / sh.HU);
-    const int grid = units < dl.sms * per_sm ? units : dl.sms * per_sm;
-    kern<<<grid, C::NT, sh.smem, stream>>>(p, map_hp, map_lp, units, sh.HU, sh.NS);
+    if (p.ckpt_hp && !encode_slab_map(&map_hp, p.ckpt_hp, false, C::P, C::N, slabs, false))
+        return cudaErrorInvalidValue;
+    // the tensor cores read bf16 column blocks
+    if (p.ckpt_lp && !encode_slab_map(&map_lp, p.ckpt_lp, true, C::P, C::N, slabs, TC))
+        return cudaErrorInvalidValue;
+    const int units = p.B * (p.H / sh.HU), ctas = (units + PIPES - 1) / PIPES;
+    const int grid = ctas < dl.sms * per_sm ? ctas : dl.sms * per_sm;
+    kern<<<grid, C::NT * PIPES, sh.smem, stream>>>(p, map_hp, map_lp, units, sh.HU, sh.NS);
     return cudaGetLastError();
+}
+
+template <class C>
+cudaError_t launch_pipe(const ReplayParams &p, cudaStream_t stream) {
+    DeviceLimits dl;
+    cudaError_t e = device_limits(dl);
+    if (e != cudaSuccess) return e;
+    if constexpr (C::UMMA) {
+        if (umma_prec<C>(p)) {
+            const LaunchShape sh = choose_shape_tc<C>(p, dl);
+            if (sh.HU != 0)
+                return sh.per_sm == 2 ? launch_kernel<C, true, 2>(p, sh, dl, stream)
+                                      : launch_kernel<C, true, 1>(p, sh, dl, stream);
+        }
+    }
+    const LaunchShape sh = choose_shape<C>(p, dl);
+    if (sh.HU == 0) return cudaErrorInvalidConfiguration;
+    return launch_kernel<C, false, 1>(p, sh, dl, stream);
 }
 
 // Verify launches instantiate the draft-count buckets 1, 4 and 8 (GDN also 3).

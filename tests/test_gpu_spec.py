@@ -57,11 +57,14 @@ def test_gdn_spec_two_precision_small_batch():
 @pytest.mark.parametrize("kind", ["mamba2", "gdn"])
 def test_two_precision_beats_shared_bf16(kind):
     """Separate precisions keep bf16 rounding out of the recurrence, so their
-    output error does not exceed that of a shared bf16 checkpoint."""
+    output error does not exceed that of a shared bf16 checkpoint.  Until a
+    sequence first folds both arms read the same bf16 values, summed in a
+    different order (tensor cores for the two-precision bf16 reads of GDN), so
+    the comparison allows a margin far below one bf16 rounding (2^-9)."""
     base = synth.WORKLOADS["gdn_spec" if kind == "gdn" else "mamba2_spec"].with_(B=6)
     e_two, _ = _run_spec(base, 24, seed=3, precision="two")
     e_shared, _ = _run_spec(base, 24, seed=3, precision="shared_bf16")
-    assert np.mean(e_two) <= np.mean(e_shared)
+    assert np.mean(e_two) <= np.mean(e_shared) * (1 + 1e-3)
 
 
 @pytest.mark.parametrize("kind", ["mamba2", "gdn"])
@@ -133,3 +136,14 @@ def test_gdn_draft_counts(T):
     """GDN rounds in every draft bucket (3, 4 and 8), fp32 checkpoint."""
     w = synth.WORKLOADS["gdn_spec"].with_(B=3, T=T, capacity=16 + T, precision="fp32", accept="uniform")
     _run_spec(w, 10, seed=13)
+
+
+@pytest.mark.parametrize("T", [1, 3, 4, 8])
+@pytest.mark.parametrize("precision", ["two", "shared_bf16"])
+def test_gdn_draft_counts_bf16(T, precision):
+    """GDN rounds in every draft bucket whose bf16 row blocks are dotted on the
+    tensor cores (1, 3, 4 and 8 drafts: 2 to 16 vectors, one or two groups of
+    the B operand), with folds of the fp32 or the bf16 copy."""
+    w = synth.WORKLOADS["gdn_spec"].with_(B=4, T=T, capacity=16 + T, precision=precision, accept="uniform")
+    _, nfold = _run_spec(w, 40 if T == 1 else 12, seed=17 + T)
+    assert nfold > 0
