@@ -140,8 +140,8 @@ struct UnitHdr {
 // consumer warps' scratch (fcf: fw_r v_r for the warp's P/NCW columns, for
 // fold_chunk(cap) records at a time).
 struct RSmem {
-    int stages, bars, plans, abort, tmem, d1, d2, sr, cst, fcf, ctx0, ctx_bytes;
-    int hdr, kraw, ar, vb, bt, c1, c2, g1, g2, fw, gF, pre1, pre2, qs, unew;  // within a context
+    int stages, bars, plans, abort, tmem, d1, d2, sr, cst, fcf, unew, ctx0, ctx_bytes;
+    int hdr, kraw, ar, vb, bt, c1, c2, g1, g2, fw, gF, pre1, pre2, qs;  // within a context
     int total;
 };
 
@@ -149,9 +149,10 @@ __host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
 
 // Units the planner lane may plan ahead of the prep warps.
 constexpr int kPlanRing = 4;
-// Records whose fold coefficients a consumer warp gathers at a time: the whole
-// window when it is at most 16 records (one gather per folded head), else 8.
-__host__ __device__ inline int fold_chunk(int cap) { return cap <= 16 ? 16 : 8; }
+// Records whose fold coefficients a consumer warp gathers at a time: 16 (a
+// fold takes at most L = 16 records, so one gather per folded head) up to a
+// 24-record buffer, else 8.
+__host__ __device__ inline int fold_chunk(int cap) { return cap <= 24 ? 16 : 8; }
 
 template <class C>
 __host__ __device__ inline RSmem replay_smem(int cap, int HU, int NS) {
@@ -169,6 +170,9 @@ __host__ __device__ inline RSmem replay_smem(int cap, int HU, int NS) {
     s.sr = o;     o += al16(HU * cap * 4);                          // Mamba-2 dt_r
     s.cst = o;    o += al16(2 * HU * 4);                            // Mamba-2 A_h, D_h
     s.fcf = o;    o += al16(fold_chunk(cap) * P * 4);               // consumer warps' fold coefficients
+    // GDN: u of this launch's records, written and read by the consumer warps
+    // (each warp its own columns) within one unit: not double-buffered
+    s.unew = o;   o += GDN ? al16(HU * TMAX * P * 4) : 0;
     int c = 0;
     s.hdr = c;    c += al16((int)sizeof(UnitHdr));
     s.kraw = c;   c += al16((cap + TMAX) * N * 2);                  // bf16 keys (rows < cap), queries (cap + i)
@@ -185,7 +189,6 @@ __host__ __device__ inline RSmem replay_smem(int cap, int HU, int NS) {
     s.pre2 = c;   c += GDN ? al16(HU * TMAX * P * 4) : 0;
     // fp32 dot vectors [QC][N][QW], or (tensor-core units) the bf16 B operand
     s.qs = c;     c += al16(C::UMMA && C::QB_BYTES > N * C::JP * 4 ? C::QB_BYTES : N * C::JP * 4);
-    s.unew = c;   c += GDN ? al16(HU * TMAX * P * 4) : 0;           // GDN: u of this launch's records
     s.ctx_bytes = c;
     s.ctx0 = o;   o += 2 * c;
     s.total = o;
@@ -971,7 +974,7 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
     uint64_t *mdone = full + 2 * NS + 6 + 2 * kPlanRing, *dfree = mdone + 2;  // tensor-core D buffers
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
     const uint16_t *kraw = reinterpret_cast<const uint16_t *>(cx + L.kraw);
-    float *unew = const_cast<float *>(reinterpret_cast<const float *>(cx + L.unew));  // GDN: u of new records
+    float *unew = reinterpret_cast<float *>(sm + L.unew);  // GDN: u of new records
     const float *ar = reinterpret_cast<const float *>(cx + L.ar);
     const uint16_t *vb = reinterpret_cast<const uint16_t *>(cx + L.vb);
     const float *bt = reinterpret_cast<const float *>(cx + L.bt);
