@@ -592,7 +592,12 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
     const int base = s.base, hc = s.hc, T = s.T, F = s.F;
     const bool append = s.append;
     const int nrec = hc + T;
-    auto slot = [&](int r) { return (base + r) % cap; };
+    // buffer slot of record r: base < cap and r < cap for every planned unit
+    // (plan_sequence), so one conditional subtract replaces the division
+    auto slot = [&](int r) {
+        const int v = base + r;
+        return v >= cap ? v - cap : v;
+    };
 
     float *d1 = reinterpret_cast<float *>(sm + L.d1), *d2 = reinterpret_cast<float *>(sm + L.d2);
     float *sr = reinterpret_cast<float *>(sm + L.sr);
@@ -968,7 +973,12 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
     const int base = s.base, hc = s.hc, T = s.T, F = s.F;
     const bool append = s.append, materialize = mode == MODE_MATERIALIZE;
     const bool keep = s.fold || materialize;  // the staged head is read again by the fold
-    auto slot = [&](int r) { return (base + r) % cap; };
+    // buffer slot of record r: base < cap and r < cap for every planned unit
+    // (plan_sequence), so one conditional subtract replaces the division
+    auto slot = [&](int r) {
+        const int v = base + r;
+        return v >= cap ? v - cap : v;
+    };
 
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + L.bars), *empty = full + NS;
     uint64_t *mdone = full + 2 * NS + 6 + 2 * kPlanRing, *dfree = mdone + 2;  // tensor-core D buffers

@@ -238,7 +238,12 @@ __device__ __forceinline__ bool consume_unit(const ReplayParams &p, uint8_t *sm,
     const bool keep = fold || materialize;  // the staged slab is needed again after the reduction
     const int J = (KIND == RS_GDN ? 2 : 1) * T;
     const int nrec = hc + T;
-    auto slot = [&](int r) { return (base + r) % cap; };
+    // buffer slot of record r: base < cap and r < cap for every planned unit
+    // (plan_sequence), so one conditional subtract replaces the division
+    auto slot = [&](int r) {
+        const int v = base + r;
+        return v >= cap ? v - cap : v;
+    };
 
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + L.bars), *empty = full + NS;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
