@@ -475,18 +475,32 @@ __device__ __forceinline__ void fold_store(const ReplayParams &p, const float (&
     }
 }
 
-// Ring position q of the stage ring: every consumer warp waits for every stage
-// in ring order and arrives once on each, after its last read; the producer
-// refills a stage only when all have.  A parity wait cannot tell a phase from
-// the one two phases later, so no warp may skip a stage or fall a ring behind.
-__device__ __forceinline__ bool wait_stage(uint64_t *full, int q, int NS, volatile int *abort_flag, uint32_t *status,
+// A position q of the stage ring as its stage (q mod NS) and the parity of
+// its fill (q div NS, mod 2), advanced incrementally (no division by the
+// run-time ring depth).  Every consumer warp waits for every stage in ring
+// order and arrives once on each, after its last read; the producer refills a
+// stage only when all have.  A parity wait cannot tell a phase from the one two
+// phases later, so no warp may skip a stage or fall a ring behind.
+struct Ring {
+    int s;
+    unsigned ph;
+};
+__device__ __forceinline__ Ring ring_add(Ring r, int n, int NS) {
+    r.s += n;
+    while (r.s >= NS) {
+        r.s -= NS;
+        r.ph ^= 1u;
+    }
+    return r;
+}
+__device__ __forceinline__ bool wait_stage(uint64_t *full, Ring q, volatile int *abort_flag, uint32_t *status,
                                            bool ok) {
-    ok = ok && wait_or_abort(full + q % NS, (unsigned)(q / NS) & 1u, abort_flag, status);
+    ok = ok && wait_or_abort(full + q.s, q.ph, abort_flag, status);
     return __all_sync(0xffffffffu, ok);
 }
-__device__ __forceinline__ void release_stage(uint64_t *empty, int q, int NS) {
+__device__ __forceinline__ void release_stage(uint64_t *empty, Ring q) {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(empty + q % NS);
+    if ((threadIdx.x & 31) == 0) mbar_arrive(empty + q.s);
 }
 
 // Fold of the lane's columns of a head whose NCB row blocks are all staged.
@@ -497,7 +511,7 @@ __device__ __forceinline__ void release_stage(uint64_t *empty, int q, int NS) {
 // block (ring position q0 + rb) is handed back as soon as its last read is
 // done, so the next copies overlap the rest of the fold.
 template <class C, typename TE>
-__device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages, int lane_off, int q0, int NS,
+__device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages, int lane_off, Ring q0, int NS,
                                           uint64_t *empty, const uint16_t *kraw,
                                           float *cfs, const FoldSrc &fs, const float *fw, float gf, int F, int j,
                                           int row0, int col0, int wcol0, int lcol, size_t goff, bool materialize,
@@ -506,7 +520,7 @@ __device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages
     constexpr int VEC = W::VEC, RK = W::RK, RGW = W::RGW, NCB = W::NCB, RB = W::RB;
     constexpr size_t RSTEP = (size_t)RGW * NCB * 128;
     const int nch = F > 0 ? (F + fc - 1) / fc : 1;
-    auto blk = [&](int rb) { return stages + (size_t)((q0 + rb) % NS) * C::STAGE + lane_off; };
+    auto blk = [&](int rb) { return stages + (size_t)ring_add(q0, rb, NS).s * C::STAGE + lane_off; };
     if constexpr (sizeof(TE) == 4) {
         for (int c = 0; c < nch; ++c) {
             const int r0 = c * fc, nr = F - r0 < fc ? F - r0 : fc;
@@ -524,7 +538,7 @@ __device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages
                     // the block is in registers; partial sums written into the
                     // stages by earlier chunks precede the copies this lets in
                     if (nch > 1) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    release_stage(empty, q0 + rb, NS);
+                    release_stage(empty, ring_add(q0, rb, NS));
                 }
                 fold_records<C, TE>(o, kraw, cfs, lcol, r0, nr > 0 ? nr : 0, rb * RB + row0);
                 if (c == nch - 1) {
@@ -545,7 +559,7 @@ __device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) o[k][e] *= gf;
             }
-            release_stage(empty, q0 + rb, NS);  // the block is in registers
+            release_stage(empty, ring_add(q0, rb, NS));  // the block is in registers
             for (int c = 0; c < nch; ++c) {
                 const int r0 = c * fc, nr = F - r0 < fc ? F - r0 : fc;
                 gather_fold_coefs<C>(cfs, fs, fw, r0, nr > 0 ? nr : 0, j, wcol0, lane);
@@ -562,7 +576,7 @@ __device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages
 // resident and stay so.  Returns false on abort.
 template <class C, typename TE, int J0>
 __device__ __forceinline__ bool head_pass(float (&acc)[WGeo<C, TE>::M], const ReplayParams &p, const uint8_t *stages,
-                                          int lane_off, int q0, int NS, uint64_t *full, uint64_t *empty,
+                                          int lane_off, Ring q0, int NS, uint64_t *full, uint64_t *empty,
                                           volatile int *abort_flag, const float *qs, int rg, bool hold) {
     using W = WGeo<C, TE>;
     bool ok = true;
@@ -570,10 +584,10 @@ __device__ __forceinline__ bool head_pass(float (&acc)[WGeo<C, TE>::M], const Re
     for (int a = 0; a < W::M; ++a) acc[a] = 0.f;
 #pragma unroll 1
     for (int rb = 0; rb < W::NCB; ++rb) {
-        const int q = q0 + rb;
-        if (!hold && !(ok = wait_stage(full, q, NS, abort_flag, p.status, ok))) break;
-        dot_rows<C, TE, J0>(stages + (size_t)(q % NS) * C::STAGE + lane_off, qs, rb * W::RB + rg, acc);
-        if (!hold) release_stage(empty, q, NS);
+        const Ring q = ring_add(q0, rb, NS);
+        if (!hold && !(ok = wait_stage(full, q, abort_flag, p.status, ok))) break;
+        dot_rows<C, TE, J0>(stages + (size_t)q.s * C::STAGE + lane_off, qs, rb * W::RB + rg, acc);
+        if (!hold) release_stage(empty, q);
     }
     return ok;
 }
@@ -962,7 +976,7 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
 template <class C, bool TC, typename TE>
 __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm, const RSmem &L, const uint8_t *cx,
                                               const SeqPlan &s, const int b, const int h0, const int HU,
-                                              const int NS, int &it, const PipeCtx &pc, int &mseq, bool &inflight) {
+                                              const int NS, Ring &it, const PipeCtx &pc, int &mseq, bool &inflight) {
     constexpr int KIND = C::KIND, P = C::P, N = C::N, TMAX = C::TMAX, JP = C::JP;
     using W = WGeo<C, TE>;
     constexpr int VEC = W::VEC, RGW = W::RGW, LR = W::LR, M = W::M, NCB = W::NCB, JN = W::JN, NPASS = W::NPASS;
@@ -1015,8 +1029,9 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
     const uint8_t *stages = sm + L.stages;
     bool ok = true;
     constexpr int VSZ = KIND == RS_MAMBA2 ? 2 : 4;
-    for (int j = 0; j < HU && ok; ++j) {
-        const int hh = h0 + j, q0 = it + j * NCB;
+    Ring q0 = it;  // the head's first row block
+    for (int j = 0; j < HU && ok; ++j, q0 = ring_add(q0, NCB, NS)) {
+        const int hh = h0 + j;
         const size_t goff = ((size_t)b * H + hh) * ((size_t)N * P);
         FoldSrc fs;
         fs.committed = static_cast<const uint8_t *>(p.buf_v) + ((size_t)b * cap * H + hh) * P * VSZ;
@@ -1030,14 +1045,14 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
         }
         fs.base = base; fs.hc = hc; fs.cap = cap;
         if (T == 0) {  // flush / materialise: fold only, the head's row blocks all resident
-            for (int rb = 0; rb < NCB && ok; ++rb) ok = wait_stage(full, q0 + rb, NS, abort_flag, p.status, ok);
+            for (int rb = 0; rb < NCB && ok; ++rb) ok = wait_stage(full, ring_add(q0, rb, NS), abort_flag, p.status, ok);
             if (!ok) break;
             fold_head<C, TE>(p, const_cast<uint8_t *>(stages), lane_off, q0, NS, empty, kraw, cfs, fs, fw, gF[j], F,
                              j, row0, col0, wcol0, lcol, goff, materialize, lane, fc);
             continue;
         }
         if (hold)
-            for (int rb = 0; rb < NCB && ok; ++rb) ok = wait_stage(full, q0 + rb, NS, abort_flag, p.status, ok);
+            for (int rb = 0; rb < NCB && ok; ++rb) ok = wait_stage(full, ring_add(q0, rb, NS), abort_flag, p.status, ok);
         if (!ok) break;
         float acc[M];
         if constexpr (KIND == RS_MAMBA2) {
@@ -1086,12 +1101,12 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
                 const uint32_t tbase = *reinterpret_cast<const volatile uint32_t *>(pc.tslot) + pc.tcol;
                 if (warp == 0) {
                     if (!hold)
-                        for (int rb = 0; rb < NCB && ok; ++rb) ok = wait_stage(full, q0 + rb, NS, abort_flag, p.status, ok);
+                        for (int rb = 0; rb < NCB && ok; ++rb) ok = wait_stage(full, ring_add(q0, rb, NS), abort_flag, p.status, ok);
                     if (ok && use > 0)
                         ok = __all_sync(0xffffffffu, wait_or_abort(dfree + db, (use - 1) & 1u, abort_flag, p.status));
                     if (ok && lane == 0) {
                         tc_fence_after_sync();
-                        const uint32_t a0 = smem_u32(stages + (size_t)(q0 % NS) * C::STAGE), b0 = smem_u32(qs);
+                        const uint32_t a0 = smem_u32(stages + (size_t)q0.s * C::STAGE), b0 = smem_u32(qs);
                         constexpr uint32_t idesc = umma_idesc_bf16(128, C::UMMA_N, true, false);
 #pragma unroll
                         for (int ks = 0; ks < N / 16; ++ks)
@@ -1112,7 +1127,7 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
                 __syncwarp();
                 if (lane == 0) mbar_arrive(dfree + db);  // this warp has read the D buffer
                 if (!hold)  // the MMAs have read the row blocks
-                    for (int rb = 0; rb < NCB; ++rb) release_stage(empty, q0 + rb, NS);
+                    for (int rb = 0; rb < NCB; ++rb) release_stage(empty, ring_add(q0, rb, NS));
                 ++mseq;
 #pragma unroll
                 for (int t = 0; t < JP; ++t) sums[t] = dv[t];
@@ -1178,10 +1193,10 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
                 fold_head<C, TE>(p, const_cast<uint8_t *>(stages), lane_off, q0, NS, empty, kraw, cfs, fs, fw, gF[j],
                                  F, j, row0, col0, wcol0, lcol, goff, materialize, lane, fc);
             else
-                for (int rb = 0; rb < NCB; ++rb) release_stage(empty, q0 + rb, NS);
+                for (int rb = 0; rb < NCB; ++rb) release_stage(empty, ring_add(q0, rb, NS));
         }
     }
-    it += HU * NCB;
+    it = q0;
     return ok;
 }
 
@@ -1232,7 +1247,7 @@ __device__ __forceinline__ void consumer_loop(const ReplayParams &p, uint8_t *sm
     uint64_t *cfull = bars + 2 * NS + 2, *cempty = cfull + 2;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
     const int lane = pc.tid & 31;
-    int it = 0;
+    Ring it = {0, 0u};
     for (int cu = 0;; ++cu) {
         const int buf = cu & 1;
         const bool ok = __all_sync(0xffffffffu, wait_or_abort(cfull + buf, (cu >> 1) & 1, abort_flag, p.status));
