@@ -521,6 +521,50 @@ __device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages
     constexpr size_t RSTEP = (size_t)RGW * NCB * 128;
     const int nch = F > 0 ? (F + fc - 1) / fc : 1;
     auto blk = [&](int rb) { return stages + (size_t)ring_add(q0, rb, NS).s * C::STAGE + lane_off; };
+    if constexpr (sizeof(TE) == 4 && W::CPW == 8 && W::RK == 8) {
+        if (nch == 1) {
+            // One gather; for the fold the lane takes 8 consecutive rows
+            // 8 rg .. 8 rg + 7 of each row block (instead of rows rg + RGW k),
+            // so that a record's keys for them are one 16-byte load.  The 8
+            // lanes of a shared-memory phase still read one whole line; the
+            // line's swizzle phase alternates with the row (NCB lines per row).
+            const int cg = lane & 7, rg = lane >> 3, cb = wcol0 / W::CBE;
+            gather_fold_coefs<C>(cfs, fs, fw, 0, F > 0 ? F : 0, j, wcol0, lane);
+            for (int rb = 0; rb < NCB; ++rb) {
+                const uint8_t *sb = stages + (size_t)ring_add(q0, rb, NS).s * C::STAGE;
+                float o[8][4];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int line = (8 * rg + k) * NCB + cb;
+                    unpack<float, 4>(ld_u4(sb + line * 128 + ((cg ^ (line & 7)) << 4)), o[k]);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[k][e] *= gf;
+                }
+                release_stage(empty, ring_add(q0, rb, NS));  // the block is in registers
+                const uint16_t *kr = kraw + rb * RB + 8 * rg;
+                for (int r = 0; r < F; ++r) {
+                    float cf[4], kv[8];
+                    load_f32_vec<4>(cfs + r * (C::P / C::NCW) + lcol, cf);
+                    unpack<uint16_t, 8>(ld_u4(kr + (size_t)r * C::N), kv);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) o[k][e] = fmaf(cf[e], kv[k], o[k][e]);
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const size_t off = goff + (size_t)(rb * RB + 8 * rg + k) * C::P + col0;
+                    if (materialize) {
+                        store_f32<4>(p.out + off, o[k]);
+                    } else {
+                        if (p.ckpt_hp) store_f32<4>(p.ckpt_hp + off, o[k]);
+                        if (p.ckpt_lp) store_bf16<4>(p.ckpt_lp + off, o[k]);
+                    }
+                }
+            }
+            return;
+        }
+    }
     if constexpr (sizeof(TE) == 4) {
         for (int c = 0; c < nch; ++c) {
             const int r0 = c * fc, nr = F - r0 < fc ? F - r0 : fc;
