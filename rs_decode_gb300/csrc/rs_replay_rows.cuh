@@ -174,9 +174,11 @@ __device__ __forceinline__ void producer(const ReplayParams &p, uint8_t *sm, con
 // Fold of one staged row block: S_new = gF S_c + sum_{r<F} (fw_r v_r) k_r^T,
 // written to the checkpoint (both copies as present) or to the materialise
 // output.  The coefficient fw_r v_r of this thread's columns is formed once per
-// record and applied to all R rows the thread owns.
+// record and applied to all R rows the thread owns.  The warp hands the stage
+// back (one arrival on `empty`) as soon as its rows are in registers, so the
+// next copy overlaps the fold's arithmetic and stores.
 template <class C, typename TE, int R, int VEC>
-__device__ __forceinline__ void fold_block(const ReplayParams &p, const TE *blk, const uint16_t *kraw,
+__device__ __forceinline__ void fold_block(const ReplayParams &p, const TE *blk, uint64_t *empty, const uint16_t *kraw,
                                            const uint16_t *xb, const float *uf, const float *fw, float gf, int F,
                                            int cap, int j, int row0, int n0p, int p0, size_t goff, bool materialize) {
     constexpr int P = C::P, N = C::N;
@@ -187,6 +189,8 @@ __device__ __forceinline__ void fold_block(const ReplayParams &p, const TE *blk,
 #pragma unroll
         for (int e = 0; e < VEC; ++e) o[k][e] *= gf;
     }
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(empty);
     for (int r = 0; r < F; ++r) {
         float cf[VEC];
         const float w = fw[j * cap + r];
@@ -550,9 +554,8 @@ __device__ __forceinline__ bool consume_unit(const ReplayParams &p, uint8_t *sm,
             for (int part = 0; part < SPLIT; ++part) {
                 const int st = (it0 + part) % NS;
                 fold_block<C, TE, R, VEC>(p, reinterpret_cast<const TE *>(sm + L.stages + (size_t)st * C::STAGE),
-                                          kraw, xb, uf, fw, gF[j], F, cap, j, part * NP, n0p, p0, goff, materialize);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty + st);
+                                          empty + st, kraw, xb, uf, fw, gF[j], F, cap, j, part * NP, n0p, p0, goff,
+                                          materialize);
             }
         }
         if (named_sync_or(1, NC, !ok)) return false;  // partials of head j complete
@@ -604,10 +607,8 @@ __device__ __forceinline__ bool consume_unit(const ReplayParams &p, uint8_t *sm,
                 for (int part = 0; part < SPLIT; ++part) {
                     const int st = (it0 + part) % NS;
                     fold_block<C, TE, R, VEC>(p, reinterpret_cast<const TE *>(sm + L.stages + (size_t)st * C::STAGE),
-                                              kraw, xb, uf, fw, gF[j], F, cap, j, part * NP, n0p, p0, goff,
-                                              materialize);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(empty + st);
+                                              empty + st, kraw, xb, uf, fw, gF[j], F, cap, j, part * NP, n0p, p0,
+                                              goff, materialize);
                 }
             }
         }
