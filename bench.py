@@ -27,6 +27,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -76,12 +77,20 @@ def measured_peaks() -> dict:
         return {}
 
 
+def _code_only(text: str) -> str:
+    """The source with comments and blank lines removed: what the compiler sees
+    (a comment edit does not change the kernel the traffic was measured on)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for name in ("rs_plan.cuh", "rs_replay_rows.cuh", "rs_replay_cols.cuh", "rs_replay.cu", "rs_replay_m2.cu",
                  "rs_replay_gdn.cu", "rs_common.cuh"):
-        with open(os.path.join(ROOT, "rs_decode_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "rs_decode_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -11,12 +11,14 @@
 // Kernel structure: a persistent, warp-specialised pipeline with three roles.
 //   * Work unit = HU heads of one sequence that share one key group.
 //   * A producer warp: one lane plans units ahead (reads a sequence's
-//     pointers, takes part in the pointer update); another streams each
-//     unit's checkpoint slabs, once the prep warps have taken up its plan,
-//     into a ring of NS shared-
-//     memory stages with tiled tensor copies (TMA) that complete on mbarriers.  A stage is one row block of a slab: 16 KiB of whole key rows
-//     (contiguous in HBM), stored with the 128-byte swizzle, so a slab takes
-//     P*sizeof(elem)/128 stages.
+//     pointers, takes part in the pointer update) and ends the pipeline with
+//     an end plan; another streams each unit's checkpoint slabs, once the prep
+//     warps have taken up its plan, into a ring of NS shared-memory stages
+//     with tiled tensor copies (TMA) that complete on mbarriers.  A stage is
+//     one row block of a slab: 16 KiB of whole key rows (contiguous in HBM),
+//     stored with the 128-byte swizzle, so a slab takes P*sizeof(elem)/128
+//     stages.  (Tensor-core launches stream the bf16 copy in column blocks
+//     instead; see the TC instantiation below.)
 //   * Three prep warps build each unit's context one unit ahead of the
 //     consumers, in a double buffer: they
 //     stage every small operand (buffered records, the step's keys / queries
@@ -40,6 +42,12 @@
 // the last unit to have read them (an arrival counter) writes the new values,
 // so no second launch is needed.  Every wait is bounded: on a time-out the CTA
 // raises RS_DEV_TIMEOUT, drains its copies and returns.
+//
+// Two instantiations per shape.  TC = false: CUDA cores only, two CTAs per SM.
+// TC = true (two-precision GDN launches): the bf16 blocks are dotted with the
+// draft vectors on the tensor cores (tcgen05.mma, accumulator in TMEM).  A
+// kernel that allocates tensor memory is resident one CTA per SM, so the TC
+// instantiation runs two pipelines side by side in one CTA.
 #pragma once
 
 #include <cuda.h>
