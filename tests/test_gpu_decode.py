@@ -145,13 +145,15 @@ def test_append_then_decode():
     assert layer.status() == 0
 
 
-@pytest.mark.parametrize("precision", ["fp32", "shared_bf16"])
+@pytest.mark.parametrize("precision", ["fp32", "shared_bf16", "two"])
 def test_gdn_long_window(precision):
     """GDN with a 32-record window: a fold takes the coefficients of its 32
     records in several gathers (fp32 checkpoints keep the partial sums in the
-    staged blocks between gathers, bf16 ones in registers)."""
+    staged blocks between gathers, bf16 ones in registers).  Two-precision
+    runs the tensor-core kernel: bf16 steps on the tensor cores, the flush step
+    on the fp32 copy with the several-gather fold."""
     w = synth.WORKLOADS["gdn"].with_(B=3, L=32)
-    _run_standard(w, 40, seed=11, precision=precision, check_materialize=(precision == "fp32"))
+    _run_standard(w, 40, seed=11, precision=precision, check_materialize=(precision != "shared_bf16"))
 
 
 def test_gdn_forced_flush_and_materialize():
