@@ -1032,7 +1032,6 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
     constexpr int KIND = C::KIND, P = C::P, N = C::N, TMAX = C::TMAX, JP = C::JP;
     using W = WGeo<C, TE>;
     constexpr int VEC = W::VEC, RGW = W::RGW, LR = W::LR, M = W::M, NCB = W::NCB, JN = W::JN, NPASS = W::NPASS;
-    constexpr int RB = W::RB;
     static_assert(NPASS == 1 || NPASS == 2 || (NPASS == 4 && KIND == RS_GDN), "passes");
     const int lane = pc.tid & 31, warp = pc.tid >> 5;
     const int H = p.H, cap = p.cap, mode = p.mode;
