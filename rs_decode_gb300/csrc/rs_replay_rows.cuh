@@ -510,19 +510,62 @@ __device__ __forceinline__ bool consume_unit(const ReplayParams &p, uint8_t *sm,
             const TE *blk = reinterpret_cast<const TE *>(sm + L.stages + (size_t)st * C::STAGE);
             if (ok && J > 0) {
                 const int row0 = part * NP + n0p;
-#pragma unroll
-                for (int k = 0; k < R; ++k) {
-                    float sv[VEC];
-                    unpack<TE, VEC>(ld_u4(blk + (size_t)(n0p + k) * P + p0), sv);
+                if constexpr (JMAX <= 2) {
+                    // the dot vectors' bf16 values at the thread's R consecutive
+                    // rows: one vector load per vector, kept packed (two values
+                    // per register) and unpacked where used
+                    static_assert(R == 2 || R == 4 || R == 8, "rows per thread");
+                    uint32_t wv[JMAX][R / 2];
 #pragma unroll
                     for (int jj = 0; jj < JMAX; ++jj) {
                         if (jj < J) {
                             // Mamba-2: q_jj ; GDN: jj < T -> k_{hc+jj}, else q_{jj-T}
-                            const int row = (KIND == RS_GDN && jj < T) ? hc + jj
-                                                                       : cap + (KIND == RS_GDN ? jj - T : jj);
-                            const float w = bf2f(kraw[(size_t)row * N + row0 + k]);
+                            const int row =
+                                (KIND == RS_GDN && jj < T) ? hc + jj : cap + (KIND == RS_GDN ? jj - T : jj);
+                            const uint16_t *src = kraw + (size_t)row * N + row0;
+                            if constexpr (R == 8) {
+                                const uint4 u = ld_u4(src);
+                                wv[jj][0] = u.x; wv[jj][1] = u.y; wv[jj][2] = u.z; wv[jj][3] = u.w;
+                            } else if constexpr (R == 4) {
+                                const uint2 u = *reinterpret_cast<const uint2 *>(src);
+                                wv[jj][0] = u.x; wv[jj][1] = u.y;
+                            } else {
+                                wv[jj][0] = *reinterpret_cast<const uint32_t *>(src);
+                            }
+                        }
+                    }
 #pragma unroll
-                            for (int e = 0; e < VEC; ++e) acc[jj][e] = fmaf(sv[e], w, acc[jj][e]);
+                    for (int k = 0; k < R; ++k) {
+                        float sv[VEC];
+                        unpack<TE, VEC>(ld_u4(blk + (size_t)(n0p + k) * P + p0), sv);
+#pragma unroll
+                        for (int jj = 0; jj < JMAX; ++jj) {
+                            if (jj < J) {
+                                const uint32_t pr = wv[jj][k >> 1];
+                                const float w =
+                                    (k & 1) ? __uint_as_float(pr & 0xffff0000u) : __uint_as_float(pr << 16);
+#pragma unroll
+                                for (int e = 0; e < VEC; ++e) acc[jj][e] = fmaf(sv[e], w, acc[jj][e]);
+                            }
+                        }
+                    }
+                } else {
+                    // more vectors: their values are read per row (fewer live
+                    // registers in the draft buckets)
+#pragma unroll
+                    for (int k = 0; k < R; ++k) {
+                        float sv[VEC];
+                        unpack<TE, VEC>(ld_u4(blk + (size_t)(n0p + k) * P + p0), sv);
+#pragma unroll
+                        for (int jj = 0; jj < JMAX; ++jj) {
+                            if (jj < J) {
+                                // Mamba-2: q_jj ; GDN: jj < T -> k_{hc+jj}, else q_{jj-T}
+                                const int row =
+                                    (KIND == RS_GDN && jj < T) ? hc + jj : cap + (KIND == RS_GDN ? jj - T : jj);
+                                const float w = bf2f(kraw[(size_t)row * N + row0 + k]);
+#pragma unroll
+                                for (int e = 0; e < VEC; ++e) acc[jj][e] = fmaf(sv[e], w, acc[jj][e]);
+                            }
                         }
                     }
                 }
