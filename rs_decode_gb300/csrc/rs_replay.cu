@@ -65,14 +65,7 @@ bool encode_slab_map(CUtensorMap *map, const void *base, bool bf16, int P, int N
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B,
-#if defined(RS_L2_PROMO) && RS_L2_PROMO == 0
-              CU_TENSOR_MAP_L2_PROMOTION_NONE,
-#elif defined(RS_L2_PROMO) && RS_L2_PROMO == 1
-              CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-#else
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-#endif
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

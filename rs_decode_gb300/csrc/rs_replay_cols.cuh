@@ -1431,16 +1431,10 @@ LaunchShape choose_shape(const ReplayParams &p, const DeviceLimits &dl) {
         const int ns_max = tier == 2 ? 8 : 12, ns_min = C::P * 4 / 128 > 4 ? C::P * 4 / 128 : 4;
         for (int HU : kHU) {
             if (hpg % HU != 0) continue;
-#if defined(RS_FORCE_HU)
-            if (HU > RS_FORCE_HU) continue;
-#endif
             const int other = replay_smem<C>(p.cap, HU, 0).total;
             int ns = (budget - other) / C::STAGE;
             if (ns > ns_max) ns = ns_max;
             if (ns < ns_min) continue;
-#if defined(RS_FORCE_NS)
-            ns = RS_FORCE_NS;
-#endif
             best = {HU, ns, tier, replay_smem<C>(p.cap, HU, ns).total + 1024};
             break;
         }

@@ -742,9 +742,6 @@ cudaError_t launch_pipe(const ReplayParams &p, cudaStream_t stream) {
 // count divides the group and whose shared memory fits.
 constexpr int kMaxSmemPerBlock = 227 * 1024;
 constexpr int kTwoPerSm = kMaxSmemPerBlock / 2 - 1024;
-#ifndef RS_DEEP_FIRST
-#define RS_DEEP_FIRST 0
-#endif
 
 template <class C>
 bool try_shape(const ReplayParams &p, int hpg, int limit, cudaStream_t s, cudaError_t &err) {
@@ -758,9 +755,7 @@ cudaError_t launch_shape(const ReplayParams &p, cudaStream_t s) {
     const int hpg = p.H / p.G;
     cudaError_t e = cudaErrorInvalidValue;
     constexpr int DEEP = 4;
-    if (!RS_DEEP_FIRST &&
-        (try_shape<PipeCfg<KIND, P, N, HUS, TMAX, NC, 2, SPLIT>>(p, hpg, kTwoPerSm, s, e) || ...))
-        return e;
+    if ((try_shape<PipeCfg<KIND, P, N, HUS, TMAX, NC, 2, SPLIT>>(p, hpg, kTwoPerSm, s, e) || ...)) return e;
     if ((try_shape<PipeCfg<KIND, P, N, HUS, TMAX, NC, DEEP, SPLIT>>(p, hpg, kMaxSmemPerBlock, s, e) || ...)) return e;
     if ((try_shape<PipeCfg<KIND, P, N, HUS, TMAX, NC, 2, SPLIT>>(p, hpg, kMaxSmemPerBlock, s, e) || ...)) return e;
     return cudaErrorInvalidConfiguration;
