@@ -140,13 +140,14 @@ struct UnitHdr {
     int b, h0;
 };
 
-// Shared-memory carve-up, byte offsets from a 1024-byte aligned base (stages
-// first, so every stage is 1024-byte aligned as the swizzle requires).  The
-// unit context (ctx*, offsets within one context) is double-buffered; the
-// prep warps' scratch (d1, d2, sr, cst) is not.  Value records (Mamba-2 x, GDN
-// u) are read from global memory where needed: a fold gathers them into the
-// consumer warps' scratch (fcf: fw_r v_r for the warp's P/NCW columns, for
-// fold_chunk(cap) records at a time).
+// Shared-memory carve-up of one pipeline, byte offsets from a 1024-byte
+// aligned base (stages first, so every stage is 1024-byte aligned as the
+// swizzle requires).  The unit context (ctx*, offsets within one context) is
+// double-buffered; the prep warps' scratch (d1, d2, sr, cst) and the consumer
+// warps' scratch (fcf, unew) are not.  Value records (Mamba-2 x, GDN u) are
+// read from global memory where needed: a fold gathers them into fcf (fw_r v_r
+// for the warp's P/NCW columns, fold_chunk(cap) records at a time); unew holds
+// the u of the launch's own records, written and read by the same warp.
 struct RSmem {
     int stages, bars, plans, abort, tmem, d1, d2, sr, cst, fcf, unew, ctx0, ctx_bytes;
     int hdr, kraw, ar, vb, bt, c1, c2, g1, g2, fw, gF, pre1, pre2, qs;  // within a context
