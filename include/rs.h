@@ -57,7 +57,7 @@ typedef enum {
     RS_OK = 0,
     RS_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or count   */
     RS_ERR_UNSUPPORTED = 2,  /* shape or mode without a kernel instantiation */
-    RS_ERR_CAPACITY = 3,     /* capacity too small for L + T_max             */
+    RS_ERR_CAPACITY = 3,     /* capacity below max(L, T_max) + T_max         */
     RS_ERR_CUDA = 4,         /* a CUDA call failed (launch or copy)          */
     RS_ERR_DEVICE = 5,       /* the device status word has bits set          */
     RS_ERR_STATIC_LIMIT = 6  /* B above RS_STATIC_MAX_SEQS (rs_decode_mamba2_noalloc) */
@@ -79,7 +79,10 @@ typedef enum {
 } rs_precision;
 
 /* Shape of one layer.  Supported (P, N): Mamba-2 (64,128), (64,64);
- * GDN (128,128), (64,64).  L >= 1, T_max in 0..8, L + T_max <= capacity <= 32. */
+ * GDN (128,128), (64,64).  L >= 1, T_max in 0..8, and
+ * max(L, T_max) + T_max <= capacity <= 32: a round of T drafts writes after
+ * the h committed records it may fold, and h reaches L (or T_max, when
+ * T_max > L, after a fully accepted round that folded). */
 typedef struct {
     int32_t kind;      /* rs_kind                                              */
     int32_t B;         /* sequences                                            */

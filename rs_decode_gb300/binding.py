@@ -129,7 +129,7 @@ def _check(fn: str, status: int) -> None:
 
 def make_desc(kind: int, B: int, H: int, G: int, P: int, N: int, L: int, T_max: int = 0,
               capacity: int | None = None, precision: int = PREC_FP32) -> LayerDesc:
-    return LayerDesc(kind, B, H, G, P, N, L, T_max, capacity if capacity else L + T_max, precision)
+    return LayerDesc(kind, B, H, G, P, N, L, T_max, capacity if capacity else max(L, T_max) + T_max, precision)
 
 
 def make_inputs(**tensors) -> Inputs:

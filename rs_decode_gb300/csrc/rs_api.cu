@@ -23,7 +23,12 @@ rs_status check_desc(const rs_layer_desc *d) {
     if (d->P < 1 || d->N < 1 || d->L < 1 || d->T_max < 0 || d->T_max > kMaxT) return RS_ERR_INVALID_ARG;
     if (d->precision < RS_PREC_FP32 || d->precision > RS_PREC_SHARED_BF16) return RS_ERR_INVALID_ARG;
     if (d->capacity > kMaxCap || d->capacity < 1) return RS_ERR_INVALID_ARG;
-    if (d->capacity < d->L + d->T_max || d->capacity < d->L) return RS_ERR_CAPACITY;
+    // A standard step needs the h <= L - 1 records since the checkpoint plus
+    // its own; a round of T drafts needs h + T, and after a fully accepted
+    // round h can be max(L, T_max) (L when h + T <= L held, T_max after a
+    // fold).  So max(L, T_max) + T_max slots always suffice, and some
+    // sequence of calls needs all of them (L + T_max when T_max <= L).
+    if (d->capacity < (d->L > d->T_max ? d->L : d->T_max) + d->T_max) return RS_ERR_CAPACITY;
     if (!replay_shape_supported(d->kind, d->P, d->N)) return RS_ERR_UNSUPPORTED;
     return RS_OK;
 }
@@ -99,7 +104,7 @@ const char *rs_status_string(rs_status s) {
         case RS_OK: return "ok";
         case RS_ERR_INVALID_ARG: return "invalid argument";
         case RS_ERR_UNSUPPORTED: return "unsupported shape or mode";
-        case RS_ERR_CAPACITY: return "buffer capacity below L + T_max";
+        case RS_ERR_CAPACITY: return "buffer capacity below max(L, T_max) + T_max";
         case RS_ERR_CUDA: return "CUDA error";
         case RS_ERR_DEVICE: return "device status bits set";
         case RS_ERR_STATIC_LIMIT: return "batch above the static scratch limit (RS_STATIC_MAX_SEQS)";

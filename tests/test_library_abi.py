@@ -79,6 +79,9 @@ def test_state_sizes(lib):
     (dict(P=48), 2),                # no kernel for this shape
     (dict(capacity=15), 3),         # below L
     (dict(T_max=4, capacity=19), 3),
+    (dict(L=2, T_max=4, capacity=6), 3),   # L + T_max, but T_max > L needs 2 T_max
+    (dict(L=2, T_max=4, capacity=8), 0),
+    (dict(L=16, T_max=4, capacity=20), 0),
     (dict(capacity=40), 1),         # above 32 slots
     (dict(T_max=9, capacity=25), 1),
     (dict(precision=7), 1),
