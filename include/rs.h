@@ -11,8 +11,8 @@
  * so that after h buffered records S = gamma * S_c + sum_j w_j v_j k_j^T,
  * with w_j the product of the decays after record j and gamma the product of
  * all of them.  A decode step appends its record and computes its output
- * straight from that form, without writing the state back; the checkpoint is
- * written only when the buffer reaches the window size L ("flush").
+ * straight from that form, without writing the state back; a new checkpoint
+ * is stored once per window, when L records have been buffered (a "flush").
  * Speculative verification appends T draft records and computes all T
  * outputs from one checkpoint read; accepting a prefix or rolling back only
  * moves pointers.

@@ -11,16 +11,16 @@ section "How it works"; the thread's post [4/N]):
 
 Rules as read from the pages:
 
-* Standard step: append one record (t = h + 1 records).  The checkpoint is
-  written only when the buffer reaches the window size L: if t >= L the step
-  folds all t records into the checkpoint (base += t, h = 0), else h = t.
+* Standard step: append one record (t = h + 1 records).  A new checkpoint is
+  stored once per window of L records: if t >= L the step folds all t
+  records into the checkpoint (base += t, h = 0), else h = t.
 * Speculative round with T drafts (flowchart on the same page): append T
   draft records; if h + T > L, fold the h committed records (drafts
-  excluded) into the checkpoint, base += h, h = 0; nd = T.  The buffer is
-  circular with capacity L + T.
-* Commit a accepted drafts: h += a, nd = 0 ("advance pointer by accepted
-  length").  Rollback: nd = 0 (a pointer move; rejected records are
-  overwritten later).
+  excluded) into the checkpoint, base += h, h = 0; nd = T.  The ring holds
+  the committed records and the drafts: L + T slots when T <= L.
+* Commit a accepted drafts: h += a, nd = 0 (the flowchart's commit moves the
+  pointer by the accepted count).  Rollback: nd = 0 (a pointer move;
+  rejected records are overwritten later).
 * Forced flush: fold the h committed records, base += h, h = 0.
 """
 from __future__ import annotations

@@ -1,5 +1,5 @@
 // Eager (load-update-store) baselines: the conventional decode step that
-// loads and stores the full state every step (the thread's post [2/N] of
+// reads and writes the whole state at each step (the thread's post [2/N] of
 // "Songlin Yang releases ReplaySSM, cutting hybrid SSM memory traffic in half
 // ..."; the abstract's "eager state management"), and the per-draft snapshot
 // scheme for speculative decoding (post [3/N] of the same thread: one state

@@ -40,8 +40,8 @@ cudaError_t init_launch(const rs_layer_desc &d, const rs_state &st, const float 
 }
 
 // ---------------------------------------------------------------- commit / rollback
-// Accepting a prefix of the drafts only advances a pointer ("Advance pointer
-// by accepted length" in the flowchart of "ReplaySSM: Cache SSM Inputs, Not
+// Accepting a prefix of the drafts only moves a pointer by the accepted count
+// (the commit box of the flowchart in "ReplaySSM: Cache SSM Inputs, Not
 // State"); rejected records stay in the buffer and are overwritten later.
 __global__ void commit_kernel(int B, const int32_t *accepted, int32_t *h, int32_t *nd, uint32_t *status) {
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
