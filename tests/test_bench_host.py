@@ -16,7 +16,6 @@ def test_code_only_sees_code_changes():
     assert bench._code_only("int x = 1;\n") != bench._code_only("int x = 2;\n")
 
 
-
 def test_algorithmic_bytes_of_the_mamba2_workload():
     """The roofline numerator at the headline shape (B=256, H=128, G=8, P=64,
     N=128, window 16), averaged over one window (h = 0..15, the 16th step
@@ -32,3 +31,32 @@ def test_algorithmic_bytes_of_the_mamba2_workload():
     assert avg == hand == 1196638208
     assert traffic.eager_step_bytes(s) == 256 * (2 * ck + inp + out)
     assert abs(avg / traffic.eager_step_bytes(s) - 0.5537) < 1e-3
+
+
+def _row(clock: str, sm: str, power: str, *active: str) -> list[str]:
+    reasons = ["Active" if n in active else "Not Active"
+               for n in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")]
+    return [f"2026/12/03 10:00:{clock}", "0", sm, "2070", power, "0x0", *reasons]
+
+
+def test_clock_summary_keeps_the_timed_window():
+    """Samples outside the timed region (with a slowdown) are left out; the
+    median SM clock, the active reasons and the peak power are of the rest."""
+    import datetime
+    rows = [_row("00.000", "1200", "300.0"),
+            _row("01.000", "2070", "1200.5", "sw_power_cap"),
+            _row("01.500", "2040", "1310.0"),
+            _row("02.000", "2060", "1250.0"),
+            _row("05.000", "900", "200.0", "hw_slowdown")]
+    t = lambda s: datetime.datetime(2026, 12, 3, 10, 0, int(s), int(round((s % 1) * 1e6))).timestamp()
+    c = bench.ClockSampler.summarise(rows, t(0.9), t(2.0))
+    assert c["samples"] == 3 and c["sm_mhz"] == 2060 and c["sm_max_mhz"] == 2070
+    assert c["reasons"] == ["sw_power_cap"] and c["power_w_max"] == 1310.0
+
+
+def test_clock_summary_without_samples_in_the_window():
+    """A run shorter than the sampling period keeps the last samples taken."""
+    rows = [_row("00.000", "2070", "800.0"), _row("00.050", "2055", "900.0", "hw_thermal_slowdown")]
+    c = bench.ClockSampler.summarise(rows, 0.0, 1.0)
+    assert c["samples"] == 2 and c["reasons"] == ["hw_thermal_slowdown"]
+    assert bench.ClockSampler.summarise([], 0.0, 1.0) is None
