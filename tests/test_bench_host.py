@@ -60,3 +60,39 @@ def test_clock_summary_without_samples_in_the_window():
     c = bench.ClockSampler.summarise(rows, 0.0, 1.0)
     assert c["samples"] == 2 and c["reasons"] == ["hw_thermal_slowdown"]
     assert bench.ClockSampler.summarise([], 0.0, 1.0) is None
+
+
+def test_algorithmic_bytes_of_the_gdn_workload():
+    """Same count for GDN decode (B=256, H_v=32, H_k=16, d=128, window 16): a
+    2 MiB checkpoint, records of u fp32 (16 KiB) + alpha (128 B) + k bf16
+    (4 KiB), inputs q, k (4 KiB each), v (8 KiB), alpha, beta (128 B each),
+    16 KiB of outputs."""
+    from rs_decode_gb300 import traffic
+    s = traffic.Shape("gdn", 256, 32, 16, 128, 128)
+    avg = sum(traffic.replay_step_bytes(s, h, flush=(h == 15)) for h in range(16)) / 16
+    rec, inp, out, ck = 16 * 1024 + 128 + 4096, 16 * 1024 + 256, 16 * 1024, 2 * 2**20
+    assert avg == 256 * (ck + ck / 16 + 7.5 * rec + 15 / 16 * rec + inp + out) == 623392768
+    assert traffic.eager_step_bytes(s) == 256 * (2 * ck + inp + out)
+
+
+def test_algorithmic_bytes_of_a_folding_verify_round():
+    """A Mamba-2 round of 4 drafts with 13 committed records (13 + 4 > 16, so
+    it folds): checkpoint read and written, 13 records read, and per draft its
+    inputs read, its record appended and its output written; the snapshot
+    baseline reads the state once and writes 4 snapshots."""
+    from rs_decode_gb300 import traffic
+    s = traffic.Shape("mamba2", 256, 128, 8, 64, 128)
+    KiB, ck = 1024, 4 * 2**20
+    assert traffic.verify_round_bytes(s, 4, 13, True, 4, 4) == ck + 13 * 19 * KiB + 4 * (20.5 + 19 + 32) * KiB + ck
+    assert traffic.snapshot_round_bytes(s, 4) == 5 * ck + 4 * (20.5 + 32) * KiB
+
+
+def test_fold_rule_of_the_byte_model_matches_the_pointer_model():
+    """The byte model's fold decision for a round is the pointer model's."""
+    from oracle.pointers import Pointers
+    from rs_decode_gb300 import traffic
+    for L in range(1, 9):
+        for T in range(1, 9):
+            for h in range(0, max(L, T) + 1):
+                p = Pointers(L, max(L, T) + T, h=h)
+                assert traffic.spec_folds(h, T, L) == (p.verify(T) > 0), (L, T, h)
