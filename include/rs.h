@@ -19,7 +19,7 @@
  *
  * ---------------------------------------------------------------- conventions
  * Ownership: the caller allocates every buffer (device memory unless stated)
- *   and passes raw pointers; rs_state_bytes() gives the sizes.  The library
+ *   and passes raw pointers; rs_state_bytes_for() gives the sizes.  The library
  *   allocates nothing and keeps no global state.  All pointers to device
  *   arrays must be 16-byte aligned.
  * Streams: every call that touches the GPU takes a stream (a cudaStream_t,
