@@ -126,3 +126,25 @@ def test_verify_rejects_draft_count_above_t_max(lib):
     # inputs of the other family are rejected
     bad = rb.Inputs(x=0x200000, dt=0x300000, A=0x400000, Bm=0x500000, Cm=0x600000, q=0x800000)
     assert lib.rs_verify(ctypes.byref(d), ctypes.byref(st), 2, ctypes.byref(bad), 0x700000, None) == 1
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without the compiled library the binding raises; there is no other
+    code path to fall back to."""
+    from rs_decode_gb300 import binding as rb
+    with pytest.raises(RuntimeError, match="librs.so not found"):
+        rb.load(str(tmp_path / "librs.so"))
+
+
+def test_product_package_does_not_reach_the_oracle():
+    """The package and the benchmark's timed path never import the oracle:
+    only tests, the smoke check and the benchmark's CPU legs may."""
+    pkg = os.path.join(ROOT, "rs_decode_gb300")
+    for name in sorted(os.listdir(pkg)):
+        if name.endswith(".py"):
+            src = open(os.path.join(pkg, name), encoding="utf-8").read()
+            assert not re.search(r"^\s*(import oracle|from oracle)", src, re.M), name
+    bench_src = open(os.path.join(ROOT, "bench.py"), encoding="utf-8").read()
+    for m in re.finditer(r"^\s*(import oracle|from oracle)", bench_src, re.M):
+        fn = [d for d in re.finditer(r"^def (\w+)", bench_src[:m.start()], re.M)][-1].group(1)
+        assert fn == "time_oracle", fn
