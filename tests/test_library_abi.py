@@ -148,3 +148,13 @@ def test_product_package_does_not_reach_the_oracle():
     for m in re.finditer(r"^\s*(import oracle|from oracle)", bench_src, re.M):
         fn = [d for d in re.finditer(r"^def (\w+)", bench_src[:m.start()], re.M)][-1].group(1)
         assert fn == "time_oracle", fn
+
+
+def test_oracle_does_not_reach_the_product():
+    """The oracle shares no code with the CUDA path: it neither imports the
+    package nor includes or loads anything of librs."""
+    odir = os.path.join(ROOT, "oracle")
+    for name in sorted(os.listdir(odir)):
+        if name.endswith((".py", ".c", ".h")):
+            src = open(os.path.join(odir, name), encoding="utf-8").read()
+            assert "rs_decode_gb300" not in src and "librs" not in src and "rs.h" not in src, name
