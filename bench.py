@@ -211,6 +211,41 @@ def time_oracle(w, seconds: float, batch: int = 16):
                       f"(H={w.H}, P={w.P}, N={w.N}), fp64 eager recurrence, {el:.1f} s"}
 
 
+def run_reference(w, K: int, W: int, budget_s: float = 120.0) -> dict:
+    """The oracle as a benchmark arm: W untimed and K timed decode steps, each
+    step one eager fp64 step of a bounded sample of the workload's sequences.
+    The sample (16 sequences, halved while the whole run would exceed
+    budget_s by a probe step's time) keeps the run within a few minutes."""
+    import oracle
+    from rs_decode_gb300 import synth
+
+    def setup(batch):
+        ws = w.with_(B=batch)
+        params = synth.layer_params(ws)
+        model = oracle.Model(ws.kind, synth.initial_state(ws), params)
+        return model, [synth.step_inputs(ws, s, params=params) for s in range(4)]
+
+    batch = 16
+    model, inputs = setup(batch)
+    t0 = time.perf_counter()
+    model.step(inputs[0])
+    probe = time.perf_counter() - t0
+    while batch > 1 and probe * (K + W) > budget_s:
+        batch //= 2
+        probe /= 2
+    model, inputs = setup(batch)
+    for s in range(W):
+        model.step(inputs[s % len(inputs)])
+    t0 = time.perf_counter()
+    for s in range(K):
+        model.step(inputs[(W + s) % len(inputs)])
+    el = time.perf_counter() - t0
+    return {"value": batch * K / el, "unit": "tokens/s", "ms_per_step": el * 1e3 / K,
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{batch} sequences per step, {K} timed decode steps after {W} warm-up steps, of the "
+                      f"{w.name} workload (H={w.H}, P={w.P}, N={w.N}), fp64 eager recurrence, {el:.1f} s"}
+
+
 # ----------------------------------------------------------------------------- GPU helpers
 def _events(n):
     import torch
@@ -612,9 +647,10 @@ def main():
             return 0
         from rs_decode_gb300 import synth
         w = synth.WORKLOADS[args.workload]
-        ref = time_oracle(w, max(2.0, args.cpu_seconds))
+        ref = run_reference(w, args.steps, args.warmup)
         line = {"impl": "reference", "metric": METRIC, "value": ref["value"], "unit": "tokens/s", "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ref["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": f"{w.kind} decode B={w.B} H={w.H} P={w.P} N={w.N} G={w.G} L={w.L}"},
                 "cpu_baseline": ref,

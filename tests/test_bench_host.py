@@ -96,3 +96,29 @@ def test_fold_rule_of_the_byte_model_matches_the_pointer_model():
             for h in range(0, max(L, T) + 1):
                 p = Pointers(L, max(L, T) + T, h=h)
                 assert traffic.spec_folds(h, T, L) == (p.verify(T) > 0), (L, T, h)
+
+
+def test_reference_arm_prints_one_line_on_rank_zero_only():
+    """`--impl reference` times the oracle for W + K steps on rank 0 and prints
+    the benchmark's JSON line; other ranks exit 0 without work."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "4", "--warmup", "3"]
+    env = dict(os.environ, WORLD_SIZE="2", RANK="1", LOCAL_RANK="1")
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == ""
+    env.update(RANK="0", LOCAL_RANK="0")
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    out = json.loads(lines[0])
+    assert out["impl"] == "reference" and out["steps"] == 4 and out["warmup"] == 3 and out["value"] > 0
+    assert out["unit"] == "tokens/s" and out["higher_is_better"] is True
+    assert out["cpu_baseline"]["kind"] == "oracle" and out["cpu_baseline"]["value"] == out["value"]
+    assert out["e2e"] == {"value": out["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                          "d2h_bytes_per_step": 0}
+    assert "4 timed decode steps after 3 warm-up steps" in out["cpu_baseline"]["sample"]

