@@ -14,6 +14,10 @@ Not State", sections "How it works" and "Limits"):
   y_t = S_t q_t + D_h x_t.
 * Gated DeltaNet: u_t = beta_t (v_t - alpha_t S_{t-1} k_t),
   S_t = alpha_t S_{t-1} + u_t k_t^T, y_t = S_t q_t.
+* Per-channel decay (a reading of Kimi Delta Attention, which section
+  "Limits" names as compatible without defining it): GDN with the scalar decay
+  replaced by one decay per key channel, D_t = S_{t-1} diag(alpha_t),
+  u_t = beta_t (v_t - D_t k_t), S_t = D_t + u_t k_t^T, y_t = S_t q_t.
 * Speculative round: the eager recurrence over the T drafts from the committed
   state; the state after the accepted prefix becomes the committed state.
 
@@ -68,6 +72,8 @@ def _load():
         lib.oracle_gdn_step.argtypes = [I, I, I, I, I] + [P] * 8
         lib.oracle_mamba2_spec_round.argtypes = [I, I, I, I, I, I] + [P] * 9
         lib.oracle_gdn_spec_round.argtypes = [I, I, I, I, I, I] + [P] * 8
+        lib.oracle_kda_step.argtypes = [I, I, I, I, I] + [P] * 8
+        lib.oracle_kda_spec_round.argtypes = [I, I, I, I, I, I] + [P] * 8
         lib.oracle_num_threads.restype = I
         _lib = lib
     return _lib
@@ -143,16 +149,49 @@ def gdn_spec_round(S: np.ndarray, q, k, v, alpha, beta, accepted) -> np.ndarray:
     return y
 
 
+# ----------------------------------------------------------------------------- per-channel decay
+def kda_step(S: np.ndarray, q, k, v, alpha, beta, want_u: bool = False):
+    """One eager step with a per-key-channel decay.  S f64[B,Hv,P,N] is
+    updated in place.  q, k u16[B,Hk,N]; v u16[B,Hv,P]; alpha f32[B,Hv,N];
+    beta f32[B,Hv].  Returns y f64[B,Hv,P] (and u f64[B,Hv,P] if asked)."""
+    B, Hv, P, N = S.shape
+    Hk = q.shape[1]
+    assert alpha.shape == (B, Hv, N), alpha.shape
+    y = np.empty((B, Hv, P), np.float64)
+    u = np.empty((B, Hv, P), np.float64) if want_u else None
+    _load().oracle_kda_step(B, Hv, Hk, P, N, _ptr(S, np.float64), _ptr(q, np.uint16),
+                            _ptr(k, np.uint16), _ptr(v, np.uint16), _ptr(alpha, np.float32),
+                            _ptr(beta, np.float32), y.ctypes.data,
+                            u.ctypes.data if want_u else None)
+    return (y, u) if want_u else y
+
+
+def kda_spec_round(S: np.ndarray, q, k, v, alpha, beta, accepted) -> np.ndarray:
+    """One speculative round with per-channel decays; q, k u16[B,T,Hk,N],
+    v u16[B,T,Hv,P], alpha f32[B,T,Hv,N], beta f32[B,T,Hv], accepted i32[B].
+    Returns y f64[B,T,Hv,P]."""
+    B, Hv, P, N = S.shape
+    T, Hk = q.shape[1], q.shape[2]
+    assert alpha.shape == (B, T, Hv, N), alpha.shape
+    y = np.empty((B, T, Hv, P), np.float64)
+    _load().oracle_kda_spec_round(B, Hv, Hk, P, N, T, _ptr(S, np.float64), _ptr(q, np.uint16),
+                                  _ptr(k, np.uint16), _ptr(v, np.uint16), _ptr(alpha, np.float32),
+                                  _ptr(beta, np.float32), _ptr(accepted, np.int32), y.ctypes.data)
+    return y
+
+
 # ----------------------------------------------------------------------------- stateful model
 class Model:
     """The eager recurrence for a batch of sequences of one layer, in fp64.
 
-    ``kind`` is "mamba2" or "gdn"; ``S0`` f32/f64[B,H,P,N]; ``params`` holds
+    ``kind`` is "mamba2", "gdn" or "kda"; ``S0`` f32/f64[B,H,P,N]; ``params`` holds
     A and D (Mamba-2).  ``step`` and ``spec_round`` take the input dicts that
     ``rs_decode_gb300.synth`` produces.
     """
 
     def __init__(self, kind: str, S0: np.ndarray, params: dict | None = None):
+        if kind not in ("mamba2", "gdn", "kda"):
+            raise ValueError(f"unknown layer kind {kind!r}")
         self.kind = kind
         self.S = np.array(S0, dtype=np.float64, order="C", copy=True)
         self.params = params or {}
@@ -161,11 +200,12 @@ class Model:
         if self.kind == "mamba2":
             return mamba2_step(self.S, d["x"], d["dt"], self.params["A"], d["Bm"], d["Cm"],
                                self.params["D"])
-        return gdn_step(self.S, d["q"], d["k"], d["v"], d["alpha"], d["beta"])
+        step = gdn_step if self.kind == "gdn" else kda_step
+        return step(self.S, d["q"], d["k"], d["v"], d["alpha"], d["beta"])
 
     def spec_round(self, d: dict) -> np.ndarray:
         if self.kind == "mamba2":
             return mamba2_spec_round(self.S, d["x"], d["dt"], self.params["A"], d["Bm"],
                                      d["Cm"], self.params["D"], d["accepted"])
-        return gdn_spec_round(self.S, d["q"], d["k"], d["v"], d["alpha"], d["beta"],
-                              d["accepted"])
+        spec = gdn_spec_round if self.kind == "gdn" else kda_spec_round
+        return spec(self.S, d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["accepted"])

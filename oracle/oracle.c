@@ -16,6 +16,13 @@
  *                 u_t = beta_t (v_t - alpha_t S_{t-1} k_t)    (section "How it works", GDN bullet)
  *                 S_t = alpha_t S_{t-1} + u_t k_t^T
  *                 y_t = S_t q_t
+ *   per-channel decay (the reading of Kimi Delta Attention, which section
+ *   "Limits" names as compatible but does not define: GDN with the scalar
+ *   alpha_t replaced by one decay per key channel, alpha_t in R^N)
+ *                 D_t = S_{t-1} diag(alpha_t)
+ *                 u_t = beta_t (v_t - D_t k_t)
+ *                 S_t = D_t + u_t k_t^T
+ *                 y_t = S_t q_t
  *
  * A speculative round (section "How it works", speculative bullet and the
  * flowchart) runs the recurrence over the T drafts from the committed state,
@@ -71,6 +78,28 @@ static void gdn_head_step(int P, int N, double *s, const uint16_t *qb, const uin
         double acc = 0.0;
         for (int n = 0; n < N; ++n) {
             row[n] = alpha * row[n] + u * bf16(kb[n]);
+            acc += row[n] * bf16(qb[n]);
+        }
+        y[p] = acc;
+        if (u_out) u_out[p] = u;
+    }
+}
+
+/* One step with a per-key-channel decay; alpha points at the head's N decays. */
+static void kda_head_step(int P, int N, double *s, const uint16_t *qb, const uint16_t *kb,
+                          const uint16_t *vb, const float *alpha, double beta, double *y, double *u_out)
+{
+    for (int p = 0; p < P; ++p) {
+        double *row = s + (size_t)p * N;
+        double dk = 0.0;
+        for (int n = 0; n < N; ++n) {
+            row[n] *= (double)alpha[n];
+            dk += row[n] * bf16(kb[n]);
+        }
+        const double u = beta * (bf16(vb[p]) - dk);
+        double acc = 0.0;
+        for (int n = 0; n < N; ++n) {
+            row[n] += u * bf16(kb[n]);
             acc += row[n] * bf16(qb[n]);
         }
         y[p] = acc;
@@ -171,6 +200,53 @@ void oracle_gdn_spec_round(int B, int Hv, int Hk, int P, int N, int T, double *S
                     const size_t bth = ((size_t)b * T + i) * Hv + h;
                     const size_t btk = ((size_t)b * T + i) * Hk + h / ratio;
                     gdn_head_step(P, N, work, q + btk * N, k + btk * N, v + bth * P, alpha[bth],
+                                  beta[bth], y + bth * P, NULL);
+                    if (i + 1 == accepted[b]) memcpy(s, work, sizeof(double) * (size_t)P * N);
+                }
+            }
+        free(work);
+    }
+}
+
+/*
+ * Per-channel-decay step.  As oracle_gdn_step, with alpha f32[B][Hv][N].
+ */
+void oracle_kda_step(int B, int Hv, int Hk, int P, int N, double *S, const uint16_t *q,
+                     const uint16_t *k, const uint16_t *v, const float *alpha, const float *beta,
+                     double *y, double *u)
+{
+    const int ratio = Hv / Hk;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < Hv; ++h) {
+            const size_t bh = (size_t)b * Hv + h, bk = (size_t)b * Hk + h / ratio;
+            kda_head_step(P, N, S + bh * P * N, q + bk * N, k + bk * N, v + bh * P, alpha + bh * N,
+                          beta[bh], y + bh * P, u ? u + bh * P : NULL);
+        }
+}
+
+/*
+ * Per-channel-decay speculative round.  As oracle_gdn_spec_round, with
+ * alpha f32[B][T][Hv][N].
+ */
+void oracle_kda_spec_round(int B, int Hv, int Hk, int P, int N, int T, double *S,
+                           const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                           const float *alpha, const float *beta, const int32_t *accepted,
+                           double *y)
+{
+    const int ratio = Hv / Hk;
+#pragma omp parallel
+    {
+        double *work = (double *)malloc(sizeof(double) * (size_t)P * N);
+#pragma omp for collapse(2) schedule(static)
+        for (int b = 0; b < B; ++b)
+            for (int h = 0; h < Hv; ++h) {
+                double *s = S + ((size_t)b * Hv + h) * P * N;
+                memcpy(work, s, sizeof(double) * (size_t)P * N);
+                for (int i = 0; i < T; ++i) {
+                    const size_t bth = ((size_t)b * T + i) * Hv + h;
+                    const size_t btk = ((size_t)b * T + i) * Hk + h / ratio;
+                    kda_head_step(P, N, work, q + btk * N, k + btk * N, v + bth * P, alpha + bth * N,
                                   beta[bth], y + bth * P, NULL);
                     if (i + 1 == accepted[b]) memcpy(s, work, sizeof(double) * (size_t)P * N);
                 }

@@ -27,6 +27,8 @@ def to_device(d: dict, device="cuda", non_blocking: bool = False) -> dict:
 class Layer:
     def __init__(self, kind: str, B: int, H: int, G: int, P: int, N: int, L: int, T_max: int = 0,
                  capacity: int | None = None, precision: int = rb.PREC_FP32, device="cuda"):
+        if kind not in ("mamba2", "gdn"):
+            raise ValueError(f"librs has no kernels for layer kind {kind!r}")
         self.kind = kind
         k = rb.MAMBA2 if kind == "mamba2" else rb.GDN
         self.desc = rb.make_desc(k, B, H, G, P, N, L, T_max, capacity, precision)

@@ -23,6 +23,9 @@ sequence per layer; "ReplaySSM: Cache SSM Inputs, Not State", sections
                 128 rounds, accepted length ~ U{0..4}.
 * ``gdn_spec``  GDN shapes of ``gdn`` at B=512, T=3, capacity 19, 128 rounds,
                 accepted length ~ Binomial(3, 0.7), two-precision checkpoint.
+* ``kda``       the shapes of ``gdn`` with one decay per key channel (a reading
+                of Kimi Delta Attention, named as compatible in section
+                "Limits" of the same page), 256 steps.
 
 Mamba-2 per step: x ~ N(0,1) bf16 [B,H,P]; B, C ~ N(0,1)/sqrt(N) bf16
 [B,G,N]; dt = softplus(N(-2, 0.5)) fp32 [B,H]; per head A = -exp(U(0, log 16))
@@ -31,6 +34,9 @@ GDN per step: q, k ~ N(0,1) rounded to bf16, L2-normalised per head in fp32
 and rounded to bf16 again [B,H_k,d]; v ~ N(0,1) bf16 [B,H_v,d];
 alpha = exp(-softplus(N(0,1)) * s_h) with s_h = exp(U(log 1, log 16)) drawn
 once per head; beta = sigmoid(N(0,1)); alpha and beta fp32 [B,H_v].
+Per-channel decay: as GDN, but alpha = exp(-softplus(N(0,1)) * s_h / 16) is
+drawn for every key channel, fp32 [B,H_v,d_k], so that over a 16-record window
+the channels of one head range from nearly forgotten to nearly kept.
 """
 from __future__ import annotations
 
@@ -42,7 +48,7 @@ import numpy as np
 # Stream identifiers (one per tensor kind).
 _ID = {
     "x": 1, "dt": 2, "Bm": 3, "Cm": 4, "A": 5, "D": 6, "S0": 7,
-    "q": 11, "k": 12, "v": 13, "alpha_n": 14, "alpha_s": 15, "beta": 16,
+    "q": 11, "k": 12, "v": 13, "alpha_n": 14, "alpha_s": 15, "beta": 16, "alpha_c": 17,
     "accept": 21,
 }
 _PARAM_STEP = 0xFFFFFFF  # "step" slot used for per-layer parameters
@@ -70,7 +76,7 @@ def _softplus(z: np.ndarray) -> np.ndarray:
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str            # "mamba2" or "gdn"
+    kind: str            # "mamba2", "gdn" or "kda" (per-channel decay)
     B: int
     H: int               # value heads (Mamba-2 heads, GDN v-heads)
     G: int               # Mamba-2 B/C groups, GDN k-heads
@@ -105,6 +111,7 @@ WORKLOADS = {
                             steps=128, T=4, capacity=20, init_std=0.1, accept="uniform"),
     "gdn_spec": Workload("gdn_spec", "gdn", B=512, H=32, G=16, P=128, N=128, L=16, steps=128,
                          T=3, capacity=19, init_std=0.1, accept="binomial0.7", precision="two"),
+    "kda": Workload("kda", "kda", B=256, H=32, G=16, P=128, N=128, L=16, steps=256, init_std=0.1),
 }
 
 
@@ -150,8 +157,12 @@ def _gdn_draw(w: Workload, seed: int, step: int, lead: tuple, params: dict) -> d
     q = _l2norm_bf16(to_bf16_bits(_rng(seed, step, "q").standard_normal(lead + (w.G, w.N), dtype=np.float32)))
     k = _l2norm_bf16(to_bf16_bits(_rng(seed, step, "k").standard_normal(lead + (w.G, w.N), dtype=np.float32)))
     v = to_bf16_bits(_rng(seed, step, "v").standard_normal(lead + (w.H, w.P), dtype=np.float32))
-    g = _softplus(_rng(seed, step, "alpha_n").standard_normal(lead + (w.H,)))
-    alpha = np.exp(-g * params["alpha_scale"].astype(np.float64)).astype(np.float32)
+    if w.kind == "kda":  # one decay per key channel
+        g = _softplus(_rng(seed, step, "alpha_c").standard_normal(lead + (w.H, w.N)))
+        alpha = np.exp(-g * params["alpha_scale"].astype(np.float64)[:, None] / 16.0).astype(np.float32)
+    else:
+        g = _softplus(_rng(seed, step, "alpha_n").standard_normal(lead + (w.H,)))
+        alpha = np.exp(-g * params["alpha_scale"].astype(np.float64)).astype(np.float32)
     beta = (1.0 / (1.0 + np.exp(-_rng(seed, step, "beta").standard_normal(lead + (w.H,))))).astype(np.float32)
     return {"q": q, "k": k, "v": v, "alpha": alpha, "beta": beta}
 
@@ -161,6 +172,7 @@ def step_inputs(w: Workload, step: int, seed: int = 0, params: dict | None = Non
 
     Mamba-2: x u16[B,H,P], dt f32[B,H], Bm u16[B,G,N], Cm u16[B,G,N].
     GDN:     q,k u16[B,G,N], v u16[B,H,P], alpha f32[B,H], beta f32[B,H].
+    kda:     as GDN with alpha f32[B,H,N].
     """
     if w.kind == "mamba2":
         return _mamba2_draw(w, seed, step, (w.B,))

@@ -6,7 +6,8 @@ None of these re-type the oracle's own loop.  They use
   exact rational arithmetic (the representation the method is built on:
   "ReplaySSM: Cache SSM Inputs, Not State", section "How it works");
 * closed forms of special cases (alpha = 1, alpha = 0, one step from zero,
-  the GDN delta-rule overwrite, beta = 0);
+  the GDN delta-rule overwrite, beta = 0; for the per-channel decay, a decay
+  equal on every channel is GDN, and a zero decay clears its key channel);
 * hand-worked examples stored in ``tests/golden/hand_worked.json``;
 * the speculative-round semantics (flowchart on the same page): outputs of a
   round equal the outputs of standard steps over the drafts, a = 0 leaves the
@@ -34,6 +35,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 
 TINY_M2 = synth.Workload("pin_m2", "mamba2", B=2, H=4, G=2, P=2, N=3, L=4, steps=6, init_std=0.5)
 TINY_GDN = synth.Workload("pin_gdn", "gdn", B=2, H=4, G=2, P=2, N=3, L=4, steps=6, init_std=0.5)
+TINY_KDA = TINY_GDN.with_(name="pin_kda", kind="kda")
 
 
 def _fr(a) -> np.ndarray:
@@ -135,6 +137,49 @@ def _unrolled_gdn(w, S0, steps):
     return ys, us
 
 
+def _unrolled_kda(w, S0, steps):
+    """Replay form with one decay per key channel, exactly.  With
+    w_j(t) = alpha_{j+1} * ... * alpha_t (elementwise over channels) and
+    gamma(t) = alpha_1 * ... * alpha_t:
+      D_t k_t = S0 (gamma(t) * k_t) + sum_{j<t} u_j ((w_j(t) * k_j) . k_t)
+      u_t = beta_t (v_t - D_t k_t)
+      y_t = S0 (gamma(t) * q_t) + sum_{j<t} u_j ((w_j(t) * k_j) . q_t) + u_t (k_t . q_t)"""
+    ratio = w.H // w.G
+    S0f = _fr(S0)
+    rec = []  # (alpha[B,H,N], u[B,H,P], k[B,H,N])
+    ys, us = [], []
+    for d in steps:
+        q_all, k_all, v_all = _bf(d["q"]), _bf(d["k"]), _bf(d["v"])
+        alpha, beta = _fr(d["alpha"]), _fr(d["beta"])
+        t = len(rec)
+        u = np.empty((w.B, w.H, w.P), dtype=object)
+        y = np.empty((w.B, w.H, w.P), dtype=object)
+        kk = np.empty((w.B, w.H, w.N), dtype=object)
+        for b in range(w.B):
+            for h in range(w.H):
+                kt, qt = k_all[b, h // ratio], q_all[b, h // ratio]
+                kk[b, h] = kt
+
+                def decay(lo):  # elementwise product of alpha_i for records lo..t (this step included)
+                    r = np.array([Fraction(1)] * w.N, dtype=object)
+                    for i in range(lo, t):
+                        r = r * rec[i][0][b, h]
+                    return r * alpha[b, h]
+
+                dk = S0f[b, h].dot(decay(0) * kt)
+                acc = S0f[b, h].dot(decay(0) * qt)
+                for j in range(t):
+                    wk = decay(j + 1) * rec[j][2][b, h]
+                    dk = dk + rec[j][1][b, h] * wk.dot(kt)
+                    acc = acc + rec[j][1][b, h] * wk.dot(qt)
+                u[b, h] = beta[b, h] * (v_all[b, h] - dk)
+                y[b, h] = acc + u[b, h] * kt.dot(qt)
+        rec.append((alpha, u, kk))
+        ys.append(y)
+        us.append(u)
+    return ys, us
+
+
 def pin_unrolled_mamba2():
     w = TINY_M2
     params = synth.layer_params(w, seed=3)
@@ -155,6 +200,20 @@ def pin_unrolled_gdn():
     S = np.array(S0, np.float64)
     for s, d in enumerate(steps):
         y, u = oracle.gdn_step(S, d["q"], d["k"], d["v"], d["alpha"], d["beta"], want_u=True)
+        _close(y, ref_y[s])
+        _close(u, ref_u[s])
+
+
+def pin_unrolled_kda():
+    w = TINY_KDA
+    params = synth.layer_params(w, seed=12)
+    S0 = synth.initial_state(w, seed=12)
+    steps = [synth.step_inputs(w, s, seed=12, params=params) for s in range(w.steps)]
+    assert steps[0]["alpha"].shape == (w.B, w.H, w.N)
+    ref_y, ref_u = _unrolled_kda(w, S0, steps)
+    S = np.array(S0, np.float64)
+    for s, d in enumerate(steps):
+        y, u = oracle.kda_step(S, d["q"], d["k"], d["v"], d["alpha"], d["beta"], want_u=True)
         _close(y, ref_y[s])
         _close(u, ref_u[s])
 
@@ -259,6 +318,68 @@ def pin_gdn_beta_zero_decays():
                                            atol=1e-15)
 
 
+def pin_kda_uniform_decay_is_gdn():
+    """A decay equal on every key channel is the scalar GDN decay: the
+    per-channel recurrence then matches the (separately pinned) GDN one."""
+    w = TINY_GDN
+    params = synth.layer_params(w, seed=13)
+    S0 = np.array(synth.initial_state(w, seed=13), np.float64)
+    Sg, Sk = S0.copy(), S0.copy()
+    for s in range(w.steps):
+        d = synth.step_inputs(w, s, seed=13, params=params)
+        a = np.ascontiguousarray(np.repeat(d["alpha"][:, :, None], w.N, axis=2))
+        yg, ug = oracle.gdn_step(Sg, d["q"], d["k"], d["v"], d["alpha"], d["beta"], want_u=True)
+        yk, uk = oracle.kda_step(Sk, d["q"], d["k"], d["v"], a, d["beta"], want_u=True)
+        np.testing.assert_allclose(yk, yg, rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(uk, ug, rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(Sk, Sg, rtol=1e-12, atol=1e-15)
+
+
+def pin_kda_beta_zero_decays_channels():
+    """beta = 0: u = 0 and S_t = S0 diag(gamma(t)), gamma(t) the elementwise
+    product of the decays; y_t = S0 (gamma(t) * q_t)."""
+    w = TINY_KDA
+    params = synth.layer_params(w, seed=14)
+    S0 = np.array(synth.initial_state(w, seed=14), np.float64)
+    S = S0.copy()
+    gamma = np.ones((w.B, w.H, w.N))
+    ratio = w.H // w.G
+    for s in range(w.steps):
+        d = synth.step_inputs(w, s, seed=14, params=params)
+        y = oracle.kda_step(S, d["q"], d["k"], d["v"], d["alpha"], np.zeros_like(d["beta"]))
+        gamma = gamma * d["alpha"].astype(np.float64)
+        np.testing.assert_allclose(S, S0 * gamma[:, :, None, :], rtol=1e-13, atol=0)
+        for b in range(w.B):
+            for h in range(w.H):
+                q = synth.bf16_bits_to_f32(d["q"][b, h // ratio]).astype(np.float64)
+                np.testing.assert_allclose(y[b, h], S0[b, h] @ (gamma[b, h] * q), rtol=1e-12, atol=1e-15)
+
+
+def pin_kda_zero_decay_clears_its_channel():
+    """alpha_t = 0 on key channel m: column m of S_t is exactly u_t k_t[m]
+    (the old column is forgotten before the rank-one update); with alpha = 1
+    elsewhere and k_t[m'] = 0 on another channel m', column m' is unchanged."""
+    w = TINY_KDA
+    params = synth.layer_params(w, seed=15)
+    S = np.array(synth.initial_state(w, seed=15), np.float64)
+    ratio = w.H // w.G
+    for s in range(w.steps):
+        d = synth.step_inputs(w, s, seed=15, params=params)
+        m, m2 = s % w.N, (s + 1) % w.N
+        d["alpha"][:] = 1.0
+        d["alpha"][:, :, m] = 0.0
+        k = synth.bf16_bits_to_f32(d["k"]).copy()
+        k[:, :, m2] = 0.0
+        d["k"] = synth.to_bf16_bits(k)
+        before = S.copy()
+        _, u = oracle.kda_step(S, d["q"], d["k"], d["v"], d["alpha"], d["beta"], want_u=True)
+        for b in range(w.B):
+            for h in range(w.H):
+                km = float(synth.bf16_bits_to_f32(d["k"][b, h // ratio])[m])
+                np.testing.assert_array_equal(S[b, h, :, m], u[b, h] * km)
+                np.testing.assert_array_equal(S[b, h, :, m2], before[b, h, :, m2])
+
+
 def pin_hand_worked():
     with open(os.path.join(HERE, "golden", "hand_worked.json")) as f:
         cases = json.load(f)["cases"]
@@ -274,9 +395,10 @@ def pin_hand_worked():
                     np.array([c["D"]], np.float32))
             else:
                 bits = lambda a: synth.to_bf16_bits(np.array([[a]], np.float32))
-                y, u = oracle.gdn_step(S, bits(st["q"]), bits(st["k"]), bits(st["v"]),
-                                       np.array([[st["alpha"]]], np.float32),
-                                       np.array([[st["beta"]]], np.float32), want_u=True)
+                step = oracle.gdn_step if c["kind"] == "gdn" else oracle.kda_step
+                y, u = step(S, bits(st["q"]), bits(st["k"]), bits(st["v"]),
+                            np.array([[st["alpha"]]], np.float32),
+                            np.array([[st["beta"]]], np.float32), want_u=True)
                 np.testing.assert_array_equal(u[0, 0], st["u"])
             np.testing.assert_array_equal(S[0, 0], np.array(st["S"], np.float64))
             np.testing.assert_array_equal(y[0, 0], st["y"])
@@ -284,7 +406,7 @@ def pin_hand_worked():
 
 # ----------------------------------------------------------------------------- speculative rounds
 def _spec_check(kind):
-    w = (TINY_M2 if kind == "mamba2" else TINY_GDN).with_(T=3, capacity=7, accept="uniform")
+    w = {"mamba2": TINY_M2, "gdn": TINY_GDN, "kda": TINY_KDA}[kind].with_(T=3, capacity=7, accept="uniform")
     params = synth.layer_params(w, seed=10)
     S0 = synth.initial_state(w, seed=10)
     spec = oracle.Model(kind, S0, params)
@@ -327,6 +449,10 @@ def pin_spec_gdn():
     _spec_check("gdn")
 
 
+def pin_spec_kda():
+    _spec_check("kda")
+
+
 def pin_spec_t1_all_accepted_is_standard():
     w = TINY_M2.with_(T=1, capacity=5, accept="uniform")
     params = synth.layer_params(w, seed=11)
@@ -344,7 +470,9 @@ def pin_spec_t1_all_accepted_is_standard():
 PINS = [pin_unrolled_mamba2, pin_unrolled_gdn, pin_mamba2_alpha_one_is_matmul,
         pin_mamba2_alpha_zero_forgets, pin_mamba2_single_step_from_zero,
         pin_gdn_delta_rule_overwrite, pin_gdn_beta_zero_decays, pin_hand_worked,
-        pin_spec_mamba2, pin_spec_gdn, pin_spec_t1_all_accepted_is_standard]
+        pin_spec_mamba2, pin_spec_gdn, pin_spec_t1_all_accepted_is_standard,
+        pin_unrolled_kda, pin_kda_uniform_decay_is_gdn, pin_kda_beta_zero_decays_channels,
+        pin_kda_zero_decay_clears_its_channel, pin_spec_kda]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -370,6 +498,14 @@ MUTATIONS = {
                                 "acc += row[n] * bf16(qb[n]);\n            row[n] = alpha * row[n] + u * bf16(kb[n]);"),
     "spec_off_by_one": ("if (i + 1 == accepted[b]) memcpy(s, work",
                         "if (i == accepted[b]) memcpy(s, work"),
+    "kda_no_decay": ("row[n] *= (double)alpha[n];\n            dk += row[n] * bf16(kb[n]);",
+                     "dk += row[n] * bf16(kb[n]);"),
+    "kda_u_from_undecayed": ("row[n] *= (double)alpha[n];\n            dk += row[n] * bf16(kb[n]);",
+                             "dk += row[n] * bf16(kb[n]);\n            row[n] *= (double)alpha[n];"),
+    "kda_channel_reversed": ("row[n] *= (double)alpha[n];", "row[n] *= (double)alpha[N - 1 - n];"),
+    "kda_decay_by_value_index": ("row[n] *= (double)alpha[n];", "row[n] *= (double)alpha[p];"),
+    "kda_no_beta": ("const double u = beta * (bf16(vb[p]) - dk);", "const double u = (bf16(vb[p]) - dk);"),
+    "kda_q_for_k": ("dk += row[n] * bf16(kb[n]);", "dk += row[n] * bf16(qb[n]);"),
 }
 
 
