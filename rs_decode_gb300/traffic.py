@@ -31,13 +31,19 @@ class Shape:
     def record_bytes(self) -> int:         # one buffered record, per sequence
         if self.kind == "mamba2":          # x bf16, dt f32, alpha f32, B bf16
             return self.H * self.P * 2 + self.H * 4 + self.H * 4 + self.G * self.N * 2
-        return self.H * self.P * 4 + self.H * 4 + self.G * self.N * 2   # u f32, alpha f32, k bf16
+        # u f32, alpha f32 (one per head, or one per key channel with a per-channel decay), k bf16
+        return self.H * self.P * 4 + self.H * self.decays * 4 + self.G * self.N * 2
 
     @property
     def input_bytes(self) -> int:          # one step's inputs, per sequence
         if self.kind == "mamba2":          # x, dt, B, C
             return self.H * self.P * 2 + self.H * 4 + 2 * self.G * self.N * 2
-        return 2 * self.G * self.N * 2 + self.H * self.P * 2 + 2 * self.H * 4   # q, k, v, alpha, beta
+        # q, k, v, alpha, beta
+        return 2 * self.G * self.N * 2 + self.H * self.P * 2 + self.H * self.decays * 4 + self.H * 4
+
+    @property
+    def decays(self) -> int:               # decays per head and record: N for a per-channel decay
+        return self.N if self.kind == "kda" else 1
 
     @property
     def y_bytes(self) -> int:

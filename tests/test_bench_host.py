@@ -122,3 +122,17 @@ def test_reference_arm_prints_one_line_on_rank_zero_only():
     assert out["e2e"] == {"value": out["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                           "d2h_bytes_per_step": 0}
     assert "4 timed decode steps after 3 warm-up steps" in out["cpu_baseline"]["sample"]
+
+
+def test_algorithmic_bytes_with_per_channel_decay():
+    """With one decay per key channel (gdn shapes), a record carries 32 x 128
+    fp32 decays (16 KiB) instead of 32, and so does a step's input: a window's
+    average step moves about 6% more than the scalar-decay GDN step."""
+    from rs_decode_gb300 import traffic
+    g = traffic.Shape("gdn", 256, 32, 16, 128, 128)
+    k = traffic.Shape("kda", 256, 32, 16, 128, 128)
+    assert k.record_bytes - g.record_bytes == k.input_bytes - g.input_bytes == 32 * 127 * 4
+    avg = lambda s: sum(traffic.replay_step_bytes(s, h, flush=(h == 15)) for h in range(16)) / 16
+    rec, inp, out, ck = 16 * 1024 + 16 * 1024 + 4096, 16 * 1024 + 16 * 1024 + 128, 16 * 1024, 2 * 2**20
+    assert avg(k) == 256 * (ck + ck / 16 + 7.5 * rec + 15 / 16 * rec + inp + out)
+    assert 1.05 < avg(k) / avg(g) < 1.08
