@@ -7,7 +7,7 @@ arithmetic lives in ``oracle.c`` (plain C, double precision, OpenMP over
 (sequence, head)), compiled here with gcc.
 
 What it computes is the conventional eager recurrence, which the method
-reproduces up to floating-point differences ("ReplaySSM: Cache SSM Inputs,
+reproduces apart from rounding ("ReplaySSM: Cache SSM Inputs,
 Not State", sections "How it works" and "Limits"):
 
 * Mamba-2: alpha_t = exp(dt_t A_h), S_t = alpha_t S_{t-1} + dt_t x_t k_t^T,

@@ -4,8 +4,8 @@
  * it; the product path never does.  It shares no code with the CUDA library.
  *
  * The method ("ReplaySSM: Cache SSM Inputs, Not State", section "How it
- * works"; abstract) produces the same outputs as conventional decoding up to
- * floating-point differences (same page, section "Limits").  So the oracle is
+ * works"; abstract) produces the outputs of conventional decoding, apart from
+ * rounding (same page, section "Limits").  So the oracle is
  * the conventional (eager) recurrence itself, in double precision, stepping a
  * fully materialised state S in R^{P x N} per (sequence, head):
  *
