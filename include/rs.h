@@ -82,7 +82,8 @@ typedef enum {
 } rs_precision;
 
 /* Shape of one layer.  Supported (P, N): Mamba-2 (64,128), (64,64);
- * GDN (128,128), (64,64).  L >= 1, T_max in 0..8, and
+ * GDN (128,128), (64,64).  1 <= B <= 65535, B * H <= 2^26 (more state than
+ * a GPU holds; kernels index slabs with 32-bit integers), L >= 1, T_max in 0..8, and
  * max(L, T_max) + T_max <= capacity <= 32: a round of T drafts writes after
  * the h committed records it may fold, and h reaches L (or T_max, when
  * T_max > L, after a fully accepted round that folded). */

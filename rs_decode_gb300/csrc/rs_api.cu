@@ -14,12 +14,17 @@ using namespace rs;
 
 namespace {
 
+constexpr long long kMaxSlabs = 1ll << 26;
+
 inline bool aligned(const void *p, size_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 rs_status check_desc(const rs_layer_desc *d) {
     if (!d) return RS_ERR_INVALID_ARG;
     if (d->kind != RS_MAMBA2 && d->kind != RS_GDN) return RS_ERR_INVALID_ARG;
     if (d->B < 1 || d->B > 65535 || d->H < 1 || d->G < 1 || d->H % d->G != 0) return RS_ERR_INVALID_ARG;
+    // kernels index slabs (sequence x head) and units with 32-bit integers; 2^26
+    // slabs of the smallest shape (64 x 64 bf16) are already 512 GiB
+    if ((long long)d->B * d->H > kMaxSlabs) return RS_ERR_INVALID_ARG;
     if (d->P < 1 || d->N < 1 || d->L < 1 || d->T_max < 0 || d->T_max > kMaxT) return RS_ERR_INVALID_ARG;
     if (d->precision < RS_PREC_FP32 || d->precision > RS_PREC_SHARED_BF16) return RS_ERR_INVALID_ARG;
     if (d->capacity > kMaxCap || d->capacity < 1) return RS_ERR_INVALID_ARG;

@@ -87,6 +87,8 @@ def test_state_sizes(lib):
     (dict(precision=7), 1),
     (dict(kind=5), 1),
     (dict(B=0), 1),
+    (dict(B=65535, H=2048, G=8), 1),  # 2^27 slabs: beyond 32-bit-safe slab indexing
+    (dict(B=65535, H=1024, G=8), 0),  # 2^26 - 2^10 slabs
 ])
 def test_descriptor_validation(lib, kw, status):
     from rs_decode_gb300 import binding as rb
