@@ -212,8 +212,9 @@ rs_status rs_materialize(const rs_layer_desc *desc, const rs_state *st, float *o
 /* ---------------------------------------------------------- eager baselines */
 /* Conventional decode that loads and stores the state every step (the
  * baseline of the thread's post [2/N] and of the abstract): S <- alpha S +
- * v k^T, y = S q (+ D x).  S: fp32 [B][H][N][P], updated in place.  Only
- * kind, B, H, G, P, N of desc are used. */
+ * v k^T, y = S q (+ D x).  S: fp32 [B][H][N][P], updated in place.  The
+ * computation uses kind, B, H, G, P, N of desc (T_max too for the snapshot
+ * calls); the whole descriptor must still pass the usual validation. */
 rs_status rs_eager_step_mamba2(const rs_layer_desc *desc, float *S, const uint16_t *x,
                                const float *dt, const float *A, const uint16_t *Bm,
                                const uint16_t *Cm, const float *D, float *y, void *stream);
