@@ -25,9 +25,11 @@
  * Streams: every call that touches the GPU takes a stream (a cudaStream_t,
  *   passed as void*; NULL = legacy default stream) and only enqueues work on
  *   it, except rs_get_status, which synchronises that stream.
- * Devices: a process drives one device.  The kernels' shared-memory opt-in
- *   is granted once per process, on the first device that launches them;
- *   calls on another device of the same process fail with RS_ERR_CUDA.
+ * Devices and threads: a process drives one device.  The kernels' shared-
+ *   memory opt-in is granted once per process, on the first device that
+ *   launches them; calls on another device of the same process fail with
+ *   RS_ERR_CUDA.  The first call of each layer shape must not run
+ *   concurrently with another host thread's call.
  * Errors: every call returns rs_status and never aborts.  Argument problems
  *   found on the host return RS_ERR_INVALID_ARG / RS_ERR_UNSUPPORTED before
  *   anything is enqueued.  A failed launch returns RS_ERR_CUDA.  Problems only
