@@ -6,8 +6,10 @@ append the step's record, replay the buffer against the checkpoint for the
 output, and (every L steps) fold the window into the checkpoint.  Headline
 workload: Mamba-2 layer, B=256 sequences, 128 heads, headdim 64, dstate 128,
 8 B/C groups, window L=16, fp32 checkpoint (4 MiB per sequence), seeded
-synthetic inputs.  The timed region covers whole windows, so flushes are
-amortised.
+synthetic inputs.  The timed region starts at a window boundary (h = 0); with
+K a multiple of L (the default, 2048) it covers whole windows, and the line
+also gives the window-weighted step (one folding launch and L - 1 streaming
+ones), so that flushes are amortised either way.
 
 Prints one JSON line: decode tokens/s (whole job), achieved HBM GB/s of the
 replay kernel against the measured peak, the eager load-update-store kernel
@@ -106,6 +108,23 @@ def profiled_traffic(workload: str) -> float | None:
     if rec.get("source_hash") != kernel_source_hash():
         return None
     return rec.get("dram_bytes_per_launch")
+
+
+def recorded_output_error() -> dict | None:
+    """The two-precision and shared-bf16 output errors of the gdn_spec workload
+    against the fp64 oracle, as the full-length parity test recorded them
+    (profiles/gdn_spec_output_error.json), if taken on the current kernel
+    source; else None.  The benchmark itself never runs the oracle on the GPU
+    workloads."""
+    path = os.path.join(ROOT, "profiles", "gdn_spec_output_error.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except OSError:
+        return None
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    return {k: rec[k] for k in ("two_precision", "shared_bf16", "metric", "sample", "test") if k in rec}
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -292,10 +311,18 @@ def measure_decode(w, K, W, dev, rank, world, want_eager=True, want_e2e=True, wa
         if world > 1:
             dist.barrier()
 
+    # W warm-up steps, then more until the window restarts (h = 0), so that the
+    # timed region begins with a whole window (the pointers move in lockstep)
     for s in range(W):
         layer.decode(dev_steps[s % npool], gp, y)
     torch.cuda.synchronize()
+    extra = (w.L - int(layer.h[0].item())) % w.L
+    for s in range(W, W + extra):
+        layer.decode(dev_steps[s % npool], gp, y)
+    torch.cuda.synchronize()
+    W += extra
     h0 = int(layer.h[0].item())
+    assert h0 == 0
     clocks = ClockSampler(dev.index or 0) if want_clocks else None
     if clocks:
         clocks.start()
@@ -341,9 +368,17 @@ def measure_decode(w, K, W, dev, rank, world, want_eager=True, want_e2e=True, wa
         nb = statistics.fmean(b for b, _ in sel)
         return {"launches": len(sel), "ms": ms, "bytes": nb, "achieved_gbs": nb / (ms * 1e-3) / 1e9}
 
+    # the window-weighted step: one folding launch and L - 1 streaming ones
+    fl, sl = split(True), split(False)
+    ww = None
+    if fl and sl:
+        ww_ms = (fl["ms"] + (w.L - 1) * sl["ms"]) / w.L
+        ww = {"ms_per_step": ww_ms, "value": w.B * world / (ww_ms * 1e-3), "unit": "tokens/s",
+              "how": f"(1 folding + {w.L - 1} streaming launches) / {w.L}, from the per-launch events"}
     out = {"ms_total": ms_total, "ms_per_step": ms_total / K, "launch_ms": statistics.fmean(launch_ms),
            "bytes_per_launch": total_bytes / K, "clock_rows": rows, "t_wall": (t_wall0, t_wall1),
-           "fold_launch": split(True), "stream_launch": split(False), "eager": None, "e2e": None}
+           "fold_launch": fl, "stream_launch": sl, "window_weighted": ww, "folds_timed": sum(f for f, _, _ in per_launch),
+           "eager": None, "e2e": None}
 
     if want_eager:
         S_e = S0.clone()
@@ -538,7 +573,7 @@ def run_sweeps(dev):
 
     def dec(w, K=256):
         m = measure_decode(w, K, 2 * w.L, dev, 0, 1, want_e2e=False, want_clocks=False)
-        gbs = m["bytes_per_launch"] / (m["launch_ms"] * 1e-3) / 1e9
+        gbs = m["bytes_per_launch"] / (m["ms_per_step"] * 1e-3) / 1e9
         return {"tokens_per_s": w.B / (m["ms_per_step"] * 1e-3), "achieved_gbs": gbs, "frac": gbs / peak,
                 "eager_tokens_per_s": m["eager"]["value"], "speedup_vs_eager": m["eager"]["speedup_of_replay"]}
 
@@ -587,7 +622,7 @@ def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
     if not args.headline_only and world == 1 and not args.batch:
         other = "gdn" if w.kind == "mamba2" else "mamba2"
         g = measure_decode(synth.WORKLOADS[other], 512, W, dev, rank, world, want_e2e=False, want_clocks=False)
-        gbs = g["bytes_per_launch"] / (g["launch_ms"] * 1e-3) / 1e9
+        gbs = g["bytes_per_launch"] / (g["ms_per_step"] * 1e-3) / 1e9
         others[other] = {"workload": f"{other} decode (shapes of the {other} workload), fp32 checkpoint",
                          "value": 256 / (g["ms_per_step"] * 1e-3), "unit": "tokens/s",
                          "ms_per_step": g["ms_per_step"], "achieved_gbs": gbs,
@@ -596,10 +631,12 @@ def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
             o = measure_spec(synth.WORKLOADS[name], 64, 8, dev, rank)
             o["frac_of_measured_peak"] = o["achieved_gbs"] / peak
             others[name] = o
+        others["gdn_spec"]["output_error_vs_oracle"] = recorded_output_error()
     if rank != 0:
         return None
 
-    achieved = m["bytes_per_launch"] / (m["launch_ms"] * 1e-3) / 1e9
+    # algorithmic bytes per launch / the timed region's time per launch
+    achieved = m["bytes_per_launch"] / (m["ms_per_step"] * 1e-3) / 1e9
     clk = ClockSampler.summarise(m["clock_rows"], *m["t_wall"]) if m["clock_rows"] else None
     kernel = {"mamba2": "rows::replay_pipe_kernel<mamba2, P=64, N=128, HU=8, TMAX=1, NC=256, NS=2, SPLIT=1>",
               "gdn": "cols::replay_pipe_kernel<gdn, P=128, N=128, TMAX=1, TC=0> (launch: HU=2, NS=5, 2 CTAs/SM)"}[w.kind]
@@ -625,10 +662,14 @@ def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
                      "frac": achieved / peak, "traffic": profiled_traffic(w.kind),
                      "peak_source": f"{peak_src} (copy bandwidth, MEASURED_PEAKS.json hbm_gbs)",
                      "algorithmic_bytes_per_launch": m["bytes_per_launch"], "kernel": kernel,
+                     "duration": "timed region / K (CUDA events on the launching stream)",
                      # the launches that fold the window (checkpoint read + write, the flush route) and
                      # the others (checkpoint read only), each against the same peak
                      "fold_launch": frac_of(m["fold_launch"], peak), "stream_launch": frac_of(m["stream_launch"], peak)},
         "hbm_gbs": achieved,
+        "timed_region": {"starts_at_window_position": 0, "folds": m["folds_timed"], "window_L": w.L,
+                         "whole_windows": K % w.L == 0},
+        "window_weighted": m["window_weighted"],
         "eager": m["eager"],
         "gpu_launches": K,
         "clocks": clk,

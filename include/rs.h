@@ -2,8 +2,19 @@
  * rs.h - C ABI of librs, a single-GPU library for the ReplaySSM decode path
  * (Mamba-2 and Gated DeltaNet layers) with hand-written sm_103a kernels.
  *
- * The method ("ReplaySSM: Cache SSM Inputs, Not State", section "How it
- * works"; the paper abstract on the same subject) keeps each sequence's
+ * Sources, cited on every declaration by a "Source:" line:
+ *   [CSI]  "ReplaySSM: Cache SSM Inputs, Not State" (a summary page): sections
+ *          "What it claims", "How it works" (its bullets and flowchart),
+ *          "Evidence" and "Limits";
+ *   [THR]  "Songlin Yang releases ReplaySSM, cutting hybrid SSM memory
+ *          traffic in half to enable 2x faster speculative decoding" (the
+ *          author's thread): posts [2/N] to [6/N] and the replies under them;
+ *   [TLDR] "ReplaySSM speeds up SSM decoding and runs in production in
+ *          GLM-5.3-Flash and Kimi-K3": its TLDR;
+ *   [ABS]  the ReplaySSM paper abstract.
+ * "Source: none" marks library plumbing that has no counterpart there.
+ *
+ * The method ([CSI] "How it works"; [ABS]) keeps each sequence's
  * recurrent state S (P x N per head) as
  *
  *     a checkpoint S_c  +  a circular buffer of the SSM inputs since S_c,
@@ -20,16 +31,18 @@
  * ---------------------------------------------------------------- conventions
  * Ownership: the caller allocates every buffer (device memory unless stated)
  *   and passes raw pointers; rs_state_bytes_for() gives the sizes.  The library
- *   allocates nothing and keeps no global state.  All pointers to device
+ *   allocates nothing and keeps no per-layer state.  All pointers to device
  *   arrays must be 16-byte aligned.
+ * State kept between calls: only per-device launch facts, each set once per
+ *   device under a lock: every kernel's dynamic shared-memory opt-in and the
+ *   device's attributes (SM count, shared-memory limits); plus the static
+ *   counters of rs_decode_mamba2_noalloc.
  * Streams: every call that touches the GPU takes a stream (a cudaStream_t,
  *   passed as void*; NULL = legacy default stream) and only enqueues work on
  *   it, except rs_get_status, which synchronises that stream.
- * Devices and threads: a process drives one device.  The kernels' shared-
- *   memory opt-in is granted once per process, on the first device that
- *   launches them; calls on another device of the same process fail with
- *   RS_ERR_CUDA.  The first call of each layer shape must not run
- *   concurrently with another host thread's call.
+ * Devices and threads: a call runs on the calling thread's current device
+ *   (device ordinals below 64).  A process may drive several devices, and
+ *   several host threads may call at once, on different layers or streams.
  * Errors: every call returns rs_status and never aborts.  Argument problems
  *   found on the host return RS_ERR_INVALID_ARG / RS_ERR_UNSUPPORTED before
  *   anything is enqueued.  A failed launch returns RS_ERR_CUDA.  Problems only
@@ -133,90 +146,121 @@ typedef struct {
 } rs_inputs;
 
 /* ------------------------------------------------------------------- host-only */
+/* Text of a status code.  Source: none (library plumbing). */
 const char *rs_status_string(rs_status s);
+/* Library name, version and target architecture.  Source: none (library plumbing). */
 const char *rs_version(void);
 /* Name and text of the CUDA error behind the calling thread's most recent
- * RS_ERR_CUDA ("" if none); for diagnostics. */
+ * RS_ERR_CUDA ("" if none); for diagnostics.  Source: none (library plumbing). */
 const char *rs_last_cuda_error(void);
 
-/* Validates the descriptor and fills the array sizes.  Host only. */
+/* Validates the descriptor and fills the byte sizes of the arrays of the
+ * per-layer state: the checkpoint in one or two precisions, the circular
+ * buffer of records (values, keys, decays), and the per-sequence pointers.
+ * Host only; out must not be NULL.
+ * Source: [CSI] "How it works", standard-decoding bullet (a checkpoint plus a
+ * buffer of the steps' (alpha, v, k) records), speculative bullet (a circular
+ * buffer of capacity L + T) and "Two precisions" bullet; [CSI] "What it
+ * claims" (an FP32 state of 4 MiB per sequence and layer). */
 rs_status rs_state_bytes_for(const rs_layer_desc *desc, rs_state_bytes *out);
 
 /* ---------------------------------------------------------------- state setup */
 /* Writes the checkpoint from init (fp32 [B][H][N][P], device; NULL = zeros):
  * the fp32 copy and/or its bf16 rounding (nearest-even) per the precision
  * mode.  Clears base, h, nd, the arrival counters and the status word.
- * This is the two-precision checkpoint writer on its own ("Two precisions"
- * bullet, section "How it works"). */
+ * This is the two-precision checkpoint writer on its own.
+ * Source: [CSI] "How it works", "Two precisions" bullet. */
 rs_status rs_init(const rs_layer_desc *desc, const rs_state *st, const float *init, void *stream);
 
 /* Reads the device status word into *bits (host), after synchronising the
- * stream; clears it if clear != 0.  Returns RS_ERR_DEVICE if any bit was set. */
+ * stream; clears it if clear != 0.  Returns RS_ERR_DEVICE if any bit was set.
+ * Source: none (library plumbing: how device-side problems reach the host). */
 rs_status rs_get_status(const rs_state *st, uint32_t *bits, int clear, void *stream);
 
 /* ------------------------------------------------------------ standard decode */
-/* One Mamba-2 decode step for all B sequences ("How it works", standard
- * decoding bullet).  Per sequence: append the record (x_t, dt_t, B_t) and
- * write y_t = gamma S_c C_t + sum_j w_j dt_j x_j (B_j . C_t) + D x_t without
- * writing the state.  When the record makes h >= L the same launch folds all
- * h records into the checkpoint, S_c <- gamma S_c + V diag(w) K^T ("flush
- * route"), and resets h to 0.  alpha_t = exp(dt_t A_h).
- * Drafts pending are dropped (RS_DEV_DRAFTS_PENDING). */
+/* One Mamba-2 decode step for all B sequences.  Per sequence: append the
+ * record (x_t, dt_t, B_t) and write y_t = gamma S_c C_t + sum_j w_j dt_j x_j
+ * (B_j . C_t) + D x_t without writing the state.  When the record makes
+ * h >= L the same launch folds all h records into the checkpoint,
+ * S_c <- gamma S_c + V diag(w) K^T (the flush route), and resets h to 0.
+ * alpha_t = exp(dt_t A_h).  Drafts pending are dropped (RS_DEV_DRAFTS_PENDING).
+ * Source: [CSI] "How it works", standard-decoding bullet; [THR] posts [4/N]
+ * and [5/N] (append instead of writing the state; the output straight from
+ * the buffer) and the replies on the flush route (the new state as one
+ * product V K^T, the output from it). */
 rs_status rs_decode_mamba2(const rs_layer_desc *desc, const rs_state *st, const uint16_t *x,
                            const float *dt, const float *A, const uint16_t *Bm,
                            const uint16_t *Cm, const float *D, float *y, void *stream);
 
-/* One Gated DeltaNet decode step ("How it works", Gated DeltaNet bullet):
- * u_t = beta_t (v_t - alpha_t S_{t-1} k_t) where S_{t-1} k_t is itself
- * replayed from the checkpoint and the buffered u_j; the record stores u_t in
- * place of v_t; y_t = S_t q_t.  One checkpoint read serves both S k and S q.
- * Flush rule as for rs_decode_mamba2. */
+/* One Gated DeltaNet decode step: u_t = beta_t (v_t - alpha_t S_{t-1} k_t)
+ * where S_{t-1} k_t is itself replayed from the checkpoint and the buffered
+ * u_j; the record stores u_t in place of v_t; y_t = S_t q_t.  One checkpoint
+ * read serves both S k and S q.  Flush rule as for rs_decode_mamba2.
+ * Source: [CSI] "How it works", Gated DeltaNet bullet. */
 rs_status rs_decode_gdn(const rs_layer_desc *desc, const rs_state *st, const uint16_t *q,
                         const uint16_t *k, const uint16_t *v, const float *alpha,
                         const float *beta, float *y, void *stream);
 
 /* ------------------------------------------------------------------ speculative */
-/* Speculative verification of T drafts (1 <= T <= T_max), either family
- * ("How it works", speculative bullet and flowchart).  Appends the T draft
- * records and writes all T outputs y [B][T][H][P] from one checkpoint read
- * and the buffer.  Per sequence, if h + T > L the committed records (never
- * the drafts) are folded into the checkpoint in the same launch (reading the
- * fp32 copy and writing both copies in two-precision mode); otherwise the
- * low-precision copy is read in two-precision mode.  Sets nd = T. */
+/* Speculative verification of T drafts (1 <= T <= T_max), either family.
+ * Appends the T draft records and writes all T outputs y [B][T][H][P] from one
+ * checkpoint read and the buffer.  Per sequence, if h + T > L the committed
+ * records (never the drafts) are folded into the checkpoint in the same
+ * launch (reading the fp32 copy and writing both copies in two-precision
+ * mode); otherwise the low-precision copy is read in two-precision mode.
+ * Sets nd = T.
+ * Source: [CSI] "How it works", speculative bullet and flowchart; [THR] post
+ * [5/N] (the output-only form turns draft verification into GEMMs). */
 rs_status rs_verify(const rs_layer_desc *desc, const rs_state *st, int T, const rs_inputs *in,
                     float *y, void *stream);
 
 /* Accepts a prefix of the drafts: h += accepted[b], nd = 0 (a pointer move).
- * accepted: device int32 [B], each in 0..nd (else clamped, RS_DEV_ACCEPT). */
+ * accepted: device int32 [B], each in 0..nd (else clamped, RS_DEV_ACCEPT).
+ * Source: [CSI] "How it works", the flowchart's last step (advance the
+ * pointer by the accepted length) and speculative bullet; [TLDR] (rolling
+ * back a wrong guess is just a pointer move). */
 rs_status rs_commit(const rs_layer_desc *desc, const rs_state *st, const int32_t *accepted,
                     void *stream);
 
-/* Discards the drafts: nd = 0.  Their records are overwritten later. */
+/* Discards the drafts: nd = 0.  Their records are overwritten later.
+ * Source: [THR] post [4/N] (rollback becomes a pointer move); [CSI] "How it
+ * works", speculative bullet (rejected records are simply overwritten). */
 rs_status rs_rollback(const rs_layer_desc *desc, const rs_state *st, void *stream);
 
 /* ---------------------------------------------------------------- maintenance */
 /* Appends n committed Mamba-2 records per sequence without computing outputs
  * or flushing (x, dt, Bm of in, each [B][n][...]).  Needs nd == 0 and
  * h + n <= capacity per sequence (else that sequence is skipped and a status
- * bit set).  GDN records depend on the state, so GDN returns RS_ERR_UNSUPPORTED. */
+ * bit set).  GDN records depend on the state, so GDN returns RS_ERR_UNSUPPORTED.
+ * Source: [CSI] "How it works", standard-decoding bullet (each step appends
+ * the token's inputs to a buffer); [THR] post [4/N]. */
 rs_status rs_append(const rs_layer_desc *desc, const rs_state *st, int n, const rs_inputs *in,
                     void *stream);
 
 /* Folds every committed record into the checkpoint now (h -> 0), writing
- * both copies in two-precision mode.  Drafts stay appended. */
+ * both copies in two-precision mode.  Drafts stay appended.
+ * Source: [CSI] "How it works", standard-decoding bullet (the checkpoint
+ * written when the window fills) and speculative bullet (flushes fold only
+ * committed records, so they may run at any time); [THR] the reply on prefix
+ * caching (a cached state must not be stale). */
 rs_status rs_flush(const rs_layer_desc *desc, const rs_state *st, void *stream);
 
 /* Writes the committed state S = gamma S_c + sum_{j<h} w_j v_j k_j^T to out
  * (fp32 [B][H][N][P], device) without changing anything; an export of the
- * current state, e.g. for prefix caching. */
+ * current state, e.g. for prefix caching.
+ * Source: [CSI] "How it works", standard-decoding bullet (the state rebuilt
+ * as the decayed checkpoint plus a sum over the buffered inputs); [THR] the
+ * reply on prefix caching. */
 rs_status rs_materialize(const rs_layer_desc *desc, const rs_state *st, float *out, void *stream);
 
 /* ---------------------------------------------------------- eager baselines */
-/* Conventional decode that loads and stores the state every step (the
- * baseline of the thread's post [2/N] and of the abstract): S <- alpha S +
- * v k^T, y = S q (+ D x).  S: fp32 [B][H][N][P], updated in place.  The
- * computation uses kind, B, H, G, P, N of desc (T_max too for the snapshot
- * calls); the whole descriptor must still pass the usual validation. */
+/* Conventional decode that loads and stores the state every step:
+ * S <- alpha S + v k^T, y = S q (+ D x).  S: fp32 [B][H][N][P], updated in
+ * place.  The computation uses kind, B, H, G, P, N of desc (T_max too for the
+ * snapshot calls); the whole descriptor must still pass the usual validation.
+ * Source: [THR] post [2/N] (loading and storing the state every step); [ABS]
+ * (eager state management); the GDN form as in [CSI] "How it works", Gated
+ * DeltaNet bullet. */
 rs_status rs_eager_step_mamba2(const rs_layer_desc *desc, float *S, const uint16_t *x,
                                const float *dt, const float *A, const uint16_t *Bm,
                                const uint16_t *Cm, const float *D, float *y, void *stream);
@@ -224,18 +268,22 @@ rs_status rs_eager_step_gdn(const rs_layer_desc *desc, float *S, const uint16_t 
                             const uint16_t *k, const uint16_t *v, const float *alpha,
                             const float *beta, float *y, void *stream);
 
-/* Per-draft snapshot baseline for speculative decoding (the thread's post
- * [3/N]: one state kept per draft token).  pool: fp32 [B][T_max+1][H][N][P];
+/* Per-draft snapshot baseline for speculative decoding: one state kept per
+ * draft token.  pool: fp32 [B][T_max+1][H][N][P];
  * cur: device int32 [B], the pool slot holding each sequence's committed state.
  * Reads slot cur[b], runs the eager recurrence over the T drafts, writes each
  * intermediate state to slot (cur[b] + 1 + i) % (T_max + 1) and the outputs to
- * y [B][T][H][P]. */
+ * y [B][T][H][P].
+ * Source: [THR] post [3/N] (a separate state for every draft token);
+ * [CSI] "Evidence" (vLLM's per-draft snapshots as the comparison). */
 rs_status rs_eager_verify_snapshots(const rs_layer_desc *desc, float *pool, const int32_t *cur,
                                     int T, const rs_inputs *in, float *y, void *stream);
 
 /* Selects the snapshot of the accepted prefix: cur[b] = (cur[b] +
  * accepted[b]) % (T_max + 1).  status (device [1], may be NULL) gets
- * RS_DEV_ACCEPT for an accepted length outside 0..T_max. */
+ * RS_DEV_ACCEPT for an accepted length outside 0..T_max.
+ * Source: [THR] post [3/N] (rolling back to the state kept for the last
+ * accepted draft). */
 rs_status rs_eager_select(const rs_layer_desc *desc, int32_t *cur, const int32_t *accepted,
                           uint32_t *status, void *stream);
 
@@ -244,21 +292,24 @@ rs_status rs_eager_select(const rs_layer_desc *desc, int32_t *cur, const int32_t
 #define RS_STATIC_MAX_SEQS 4096
 
 /* rs_decode_mamba2 for callers that cannot give the library any device memory
- * beyond inputs, outputs and the layer state (no counterpart in the paper: it
- * is a packaging choice).  Examples are an engine plugin that only receives
- * pre-planned tensors, or a server that forbids device allocation after
- * start-up.  The per-sequence arrival counters, which rs_decode_mamba2 keeps in
- * st->arrive (that member is ignored here and may be NULL), live in a 16 KiB
- * static device array of this library instead.
+ * beyond inputs, outputs and the layer state.  Examples are an engine plugin
+ * that only receives pre-planned tensors, or a server that forbids device
+ * allocation after start-up.  The per-sequence arrival counters, which
+ * rs_decode_mamba2 keeps in st->arrive (that member is ignored here and may be
+ * NULL), live in a 16 KiB static device array of this library instead.
  *   - B <= RS_STATIC_MAX_SEQS, else RS_ERR_STATIC_LIMIT and nothing is enqueued.
- *   - The first call on a device looks up the array's address with that device
- *     current; make it before any stream capture.  Each call clears the
- *     counters it uses on `stream`, then runs the same kernel as
- *     rs_decode_mamba2 with the same results.
+ *   - The first call in a device context looks up the array's address with
+ *     that device current; make it before any stream capture.  The address is
+ *     tagged with the context's unique ID, so the first call in a new context
+ *     of the device (after cudaDeviceReset, say) looks it up again and
+ *     should come before any capture too.  Each call clears the counters it
+ *     uses on `stream`, then runs the same kernel as rs_decode_mamba2 with the
+ *     same results.
  *   - All calls share the array: calls that overlap on the GPU race, so
  *     serialise them.  The array stays allocated on every device that loaded
  *     the library until the process exits.
- *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * Source: none (no counterpart in the paper: a packaging choice). */
 rs_status rs_decode_mamba2_noalloc(const rs_layer_desc *desc, const rs_state *st, const uint16_t *x,
                                    const float *dt, const float *A, const uint16_t *Bm,
                                    const uint16_t *Cm, const float *D, float *y, void *stream);

@@ -1,6 +1,7 @@
 // C-ABI entry points of librs: argument validation on the host, then one or
 // two kernel launches on the caller's stream.  No entry point allocates
-// memory or keeps state between calls.
+// memory; between calls the library keeps only per-device launch facts (the
+// kernels' shared-memory opt-in and the device's attributes).
 #include <stdint.h>
 #include <stdio.h>
 
@@ -17,6 +18,12 @@ namespace {
 constexpr long long kMaxSlabs = 1ll << 26;
 
 inline bool aligned(const void *p, size_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+thread_local char g_last_cuda_error[160] = "";
+
+}  // namespace
+
+namespace rs {
 
 rs_status check_desc(const rs_layer_desc *d) {
     if (!d) return RS_ERR_INVALID_ARG;
@@ -38,7 +45,7 @@ rs_status check_desc(const rs_layer_desc *d) {
     return RS_OK;
 }
 
-rs_status check_state(const rs_layer_desc *d, const rs_state *s) {
+rs_status check_state(const rs_layer_desc *d, const rs_state *s, bool need_arrive) {
     if (!s) return RS_ERR_INVALID_ARG;
     const bool need_hp = d->precision != RS_PREC_SHARED_BF16, need_lp = d->precision != RS_PREC_FP32;
     if (need_hp != (s->ckpt_hp != nullptr) || need_lp != (s->ckpt_lp != nullptr)) return RS_ERR_INVALID_ARG;
@@ -47,28 +54,16 @@ rs_status check_state(const rs_layer_desc *d, const rs_state *s) {
     if (!aligned(s->buf_v, 16) || !aligned(s->buf_k, 16) || !aligned(s->buf_a, 4)) return RS_ERR_INVALID_ARG;
     if ((d->kind == RS_MAMBA2) != (s->buf_s != nullptr)) return RS_ERR_INVALID_ARG;
     if (s->buf_s && !aligned(s->buf_s, 4)) return RS_ERR_INVALID_ARG;
-    if (!aligned(s->base, 4) || !aligned(s->h, 4) || !aligned(s->nd, 4) || !aligned(s->arrive, 4) ||
-        !aligned(s->status, 4))
+    if (!aligned(s->base, 4) || !aligned(s->h, 4) || !aligned(s->nd, 4) || !aligned(s->status, 4))
         return RS_ERR_INVALID_ARG;
+    if (need_arrive && !aligned(s->arrive, 4)) return RS_ERR_INVALID_ARG;
     return RS_OK;
 }
-
-thread_local char g_last_cuda_error[160] = "";
 
 rs_status cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return RS_OK;
     snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
     return RS_ERR_CUDA;
-}
-
-ReplayParams replay_params(const rs_layer_desc *d, const rs_state *s, int mode, int T) {
-    ReplayParams p = {};
-    p.B = d->B; p.H = d->H; p.G = d->G; p.L = d->L; p.cap = d->capacity; p.T = T;
-    p.prec = d->precision; p.mode = mode;
-    p.ckpt_hp = s->ckpt_hp; p.ckpt_lp = s->ckpt_lp;
-    p.buf_v = s->buf_v; p.buf_k = s->buf_k; p.buf_a = s->buf_a; p.buf_s = s->buf_s;
-    p.base = s->base; p.h = s->h; p.nd = s->nd; p.arrive = s->arrive; p.status = s->status;
-    return p;
 }
 
 // Inputs of one family; all other members must be null.
@@ -89,10 +84,25 @@ rs_status check_inputs(int kind, const rs_inputs *in, bool need_q) {
     return RS_OK;
 }
 
+}  // namespace rs
+
+namespace {
+
+ReplayParams replay_params(const rs_layer_desc *d, const rs_state *s, int mode, int T) {
+    ReplayParams p = {};
+    p.B = d->B; p.H = d->H; p.G = d->G; p.L = d->L; p.cap = d->capacity; p.T = T;
+    p.prec = d->precision; p.mode = mode;
+    p.ckpt_hp = s->ckpt_hp; p.ckpt_lp = s->ckpt_lp;
+    p.buf_v = s->buf_v; p.buf_k = s->buf_k; p.buf_a = s->buf_a; p.buf_s = s->buf_s;
+    p.base = s->base; p.h = s->h; p.nd = s->nd; p.arrive = s->arrive; p.status = s->status;
+    return p;
+}
+
 void set_inputs(ReplayParams &p, const rs_inputs &in) {
     p.x = in.x; p.dt = in.dt; p.A = in.A; p.Bm = in.Bm; p.Cm = in.Cm; p.D = in.D;
     p.q = in.q; p.k = in.k; p.v = in.v; p.alpha = in.alpha; p.beta = in.beta;
 }
+
 
 #define RS_TRY(expr)                      \
     do {                                  \

@@ -57,8 +57,12 @@ __device__ __forceinline__ unsigned zero_dependent_on(unsigned x) {
 // ---------------------------------------------------------------- mbarriers and bulk copies
 // Shared-memory transaction barriers and the bulk (TMA) copy engine, used by
 // the streaming pipeline.  Every wait is bounded: after kWaitLimitNs of
-// global time it gives up and returns false, so no launch can hang.
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+// global time it gives up and returns false, so no launch can hang.  A build
+// may shorten the limit (-DRS_WAIT_LIMIT_NS=...), as the time-out test does.
+#ifndef RS_WAIT_LIMIT_NS
+#define RS_WAIT_LIMIT_NS 2000000000ull  // 2 s
+#endif
+constexpr unsigned long long kWaitLimitNs = RS_WAIT_LIMIT_NS;
 
 __device__ __forceinline__ unsigned smem_u32(const void *p) { return (unsigned)__cvta_generic_to_shared(p); }
 

@@ -181,12 +181,9 @@ static cudaError_t launch_eager(const EagerParams &p, cudaStream_t s) {
                           (NT / 32) * HPC * J1 * P;
     const size_t smem = floats * sizeof(float);
     auto kern = eager_kernel<KIND, P, N, HPC, NT>;
-    static int smem_set = 0;
-    if ((int)smem > smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        smem_set = (int)smem;
-    }
+    static SmemGrants grants;  // this instantiation's opt-in, per device
+    const cudaError_t e = grant_smem(reinterpret_cast<const void *>(kern), (int)smem, grants);
+    if (e != cudaSuccess) return e;
     kern<<<dim3(p.H / HPC, p.B), NT, smem, s>>>(p);
     return cudaGetLastError();
 }

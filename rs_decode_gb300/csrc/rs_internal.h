@@ -5,9 +5,50 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "rs.h"
 
 namespace rs {
+
+// Devices a process may drive through the library (ordinals 0 .. kMaxDevices-1).
+constexpr int kMaxDevices = 64;
+
+// Dynamic shared-memory opt-in of one kernel instantiation, per device.
+// cudaFuncSetAttribute acts on the current device only, so each device gets
+// its own grant; the mutex makes the first launches from several host threads
+// safe.  This (and the per-device attribute cache of the column-split launcher)
+// is the only state the library keeps between calls.
+struct SmemGrants {
+    std::mutex mu;
+    int bytes[kMaxDevices] = {};
+};
+
+// Grants `kern` at least `smem` bytes of dynamic shared memory on the current
+// device (once per device and size).
+inline cudaError_t grant_smem(const void *kern, int smem, SmemGrants &g) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g.mu);
+    if (g.bytes[dev] < smem) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        g.bytes[dev] = smem;
+    }
+    return cudaSuccess;
+}
+
+// Host-side checks shared by the entry points (rs_api.cu).  check_state with
+// need_arrive = false ignores the arrival-counter array (the entry point that
+// keeps its own counters).
+rs_status check_desc(const rs_layer_desc *d);
+rs_status check_state(const rs_layer_desc *d, const rs_state *s, bool need_arrive = true);
+rs_status check_inputs(int kind, const rs_inputs *in, bool need_q);
+// RS_OK for cudaSuccess; otherwise records the error's name and text for
+// rs_last_cuda_error (per host thread) and returns RS_ERR_CUDA.
+rs_status cuda_status(cudaError_t e);
 
 // Arguments of the replay kernels (decode, verify, flush, materialise).
 struct ReplayParams {

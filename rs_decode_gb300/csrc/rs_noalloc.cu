@@ -15,9 +15,11 @@
 //    RS_ERR_STATIC_LIMIT before anything is enqueued;
 //  * the array exists once per device that loads the library and lives until
 //    the process exits (16 KiB);
-//  * the first call on a device looks up the array's device address
+//  * the first call in a device context looks up the array's device address
 //    (cudaGetSymbolAddress) with that device current; make that first call
-//    before any stream capture;
+//    before any stream capture.  The address is cached per device and tagged
+//    with the context's unique ID, so a call in a new context of the device
+//    (after cudaDeviceReset, say) looks it up again;
 //  * every call clears the counters it uses (cudaMemsetAsync on the caller's
 //    stream) and then launches the same kernel as rs_decode_mamba2;
 //  * all calls share the one array, so calls that overlap on the GPU (other
@@ -25,6 +27,7 @@
 //  * no cudaMalloc, cudaFree or allocating library routine is called.
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "rs.h"
@@ -34,57 +37,85 @@
 namespace {
 
 constexpr int kStaticMaxSeqs = RS_STATIC_MAX_SEQS;
-constexpr int kMaxDevices = 64;
 
 // Zero-initialised when the module loads on a device; cleared again per call.
 static __device__ __align__(256) uint32_t g_arrive[kStaticMaxSeqs];
 
-std::mutex g_mu;
-uint32_t *g_arrive_addr[kMaxDevices] = {};
+// The current context's unique ID (cuCtxGetCurrent + cuCtxGetId, fetched from
+// the driver through the runtime: no link-time dependency on the driver
+// library).  0 when it cannot be read.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
 
-// Device address of g_arrive on the current device (looked up once per device).
-rs_status static_arrive(uint32_t **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return RS_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return RS_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_arrive_addr[dev]) {
-        void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_arrive) != cudaSuccess || !ptr) return RS_ERR_CUDA;
-        g_arrive_addr[dev] = static_cast<uint32_t *>(ptr);
-    }
-    *out = g_arrive_addr[dev];
-    return RS_OK;
+template <class Fn>
+Fn driver_fn(const char *name) {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(f);
 }
 
-inline bool aligned(const void *p, size_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+unsigned long long current_context_id() {
+    static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+struct ArriveAddr {
+    unsigned long long ctx_id;  // context the address was looked up in
+    uint32_t *addr;
+};
+
+std::mutex g_mu;
+ArriveAddr g_arrive_addr[rs::kMaxDevices] = {};
+
+// Device address of g_arrive on the current device, looked up once per device
+// context.
+rs_status static_arrive(uint32_t **out) {
+    int dev = 0;
+    rs_status st = rs::cuda_status(cudaGetDevice(&dev));
+    if (st != RS_OK) return st;
+    if (dev < 0 || dev >= rs::kMaxDevices) return RS_ERR_UNSUPPORTED;
+    const unsigned long long ctx = current_context_id();
+    std::lock_guard<std::mutex> lock(g_mu);
+    ArriveAddr &a = g_arrive_addr[dev];
+    if (!a.addr || ctx == 0 || a.ctx_id != ctx) {
+        void *ptr = nullptr;
+        st = rs::cuda_status(cudaGetSymbolAddress(&ptr, g_arrive));
+        if (st != RS_OK) return st;
+        if (!ptr) return RS_ERR_CUDA;
+        a.addr = static_cast<uint32_t *>(ptr);
+        a.ctx_id = ctx;
+    }
+    *out = a.addr;
+    return RS_OK;
+}
 
 }  // namespace
 
 extern "C" rs_status rs_decode_mamba2_noalloc(const rs_layer_desc *d, const rs_state *st, const uint16_t *x,
                                               const float *dt, const float *A, const uint16_t *Bm,
                                               const uint16_t *Cm, const float *D, float *y, void *stream) {
-    rs_state_bytes sizes;
-    const rs_status ds = rs_state_bytes_for(d, &sizes);  // validates the descriptor
-    if (ds != RS_OK) return ds;
+    rs_status s = rs::check_desc(d);
+    if (s != RS_OK) return s;
     if (d->kind != RS_MAMBA2) return RS_ERR_INVALID_ARG;
     if (d->B > kStaticMaxSeqs) return RS_ERR_STATIC_LIMIT;
-    if (!st) return RS_ERR_INVALID_ARG;
-    const bool need_hp = d->precision != RS_PREC_SHARED_BF16, need_lp = d->precision != RS_PREC_FP32;
-    if (need_hp != (st->ckpt_hp != nullptr) || need_lp != (st->ckpt_lp != nullptr)) return RS_ERR_INVALID_ARG;
-    if ((need_hp && !aligned(st->ckpt_hp, 16)) || (need_lp && !aligned(st->ckpt_lp, 16))) return RS_ERR_INVALID_ARG;
-    if (!aligned(st->buf_v, 16) || !aligned(st->buf_k, 16) || !aligned(st->buf_a, 4) || !aligned(st->buf_s, 4) ||
-        !aligned(st->base, 4) || !aligned(st->h, 4) || !aligned(st->nd, 4) || !aligned(st->status, 4))
-        return RS_ERR_INVALID_ARG;
-    if (!aligned(x, 16) || !aligned(dt, 4) || !aligned(A, 4) || !aligned(Bm, 16) || !aligned(Cm, 16) ||
-        (D && !aligned(D, 4)) || !aligned(y, 16))
-        return RS_ERR_INVALID_ARG;
+    if ((s = rs::check_state(d, st, /*need_arrive=*/false)) != RS_OK) return s;
+    rs_inputs in = {};
+    in.x = x; in.dt = dt; in.A = A; in.Bm = Bm; in.Cm = Cm; in.D = D;
+    if ((s = rs::check_inputs(RS_MAMBA2, &in, true)) != RS_OK) return s;
+    if (!y || (reinterpret_cast<uintptr_t>(y) & 15) != 0) return RS_ERR_INVALID_ARG;
 
     uint32_t *arrive = nullptr;
-    const rs_status as = static_arrive(&arrive);
-    if (as != RS_OK) return as;
-    cudaStream_t s = (cudaStream_t)stream;
-    if (cudaMemsetAsync(arrive, 0, sizeof(uint32_t) * (size_t)d->B, s) != cudaSuccess) return RS_ERR_CUDA;
+    if ((s = static_arrive(&arrive)) != RS_OK) return s;
+    cudaStream_t cs = (cudaStream_t)stream;
+    if ((s = rs::cuda_status(cudaMemsetAsync(arrive, 0, sizeof(uint32_t) * (size_t)d->B, cs))) != RS_OK) return s;
 
     rs::ReplayParams p = {};
     p.B = d->B; p.H = d->H; p.G = d->G; p.L = d->L; p.cap = d->capacity; p.T = 1;
@@ -93,5 +124,5 @@ extern "C" rs_status rs_decode_mamba2_noalloc(const rs_layer_desc *d, const rs_s
     p.buf_v = st->buf_v; p.buf_k = st->buf_k; p.buf_a = st->buf_a; p.buf_s = st->buf_s;
     p.base = st->base; p.h = st->h; p.nd = st->nd; p.arrive = arrive; p.status = st->status;
     p.x = x; p.dt = dt; p.A = A; p.Bm = Bm; p.Cm = Cm; p.D = D; p.y = y;
-    return rs::replay_launch(p, d->kind, d->P, d->N, s) == cudaSuccess ? RS_OK : RS_ERR_CUDA;
+    return rs::cuda_status(rs::replay_launch(p, d->kind, d->P, d->N, cs));
 }

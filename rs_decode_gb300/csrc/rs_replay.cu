@@ -42,7 +42,6 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-constexpr int kMaxDevices = 64;
 DeviceLimits g_limits[kMaxDevices];
 bool g_limits_ok[kMaxDevices];
 std::mutex g_limits_mu;

@@ -1472,13 +1472,9 @@ template <class C, bool TC, int PIPES>
 cudaError_t launch_kernel(const ReplayParams &p, const LaunchShape &sh, const DeviceLimits &dl,
                           cudaStream_t stream) {
     auto kern = replay_pipe_kernel<C, TC, PIPES>;
-    static bool attr_set = false;
-    cudaError_t e;
-    if (!attr_set) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dl.smem_per_block);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static SmemGrants grants;  // this instantiation's opt-in, per device
+    cudaError_t e = grant_smem(reinterpret_cast<const void *>(kern), dl.smem_per_block, grants);
+    if (e != cudaSuccess) return e;
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::NT * PIPES, sh.smem);
     if (e != cudaSuccess) return e;

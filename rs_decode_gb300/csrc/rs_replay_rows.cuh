@@ -712,21 +712,14 @@ cudaError_t launch_pipe(const ReplayParams &p, cudaStream_t stream) {
     const PipeSmem L = pipe_smem<C>(p.cap);
     const int smem = L.total;
     auto kern = replay_pipe_kernel<C>;
-    static int smem_set = 0;  // largest opt-in already granted to this instantiation
-    static int per_sm = 0;
-    if (smem > smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        smem_set = smem;
-        per_sm = 0;
-    }
-    if (per_sm == 0) {
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::NT, smem);
-        if (e != cudaSuccess) return e;
-        if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    }
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static SmemGrants grants;  // this instantiation's opt-in, per device
+    cudaError_t e = grant_smem(reinterpret_cast<const void *>(kern), smem, grants);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0, dev = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::NT, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const int units = p.B * (p.H / C::HU);

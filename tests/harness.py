@@ -33,6 +33,44 @@ def rel_err(got, ref) -> np.ndarray:
     return np.max(np.abs(g - r), axis=1) / np.maximum(np.max(np.abs(r), axis=1), 1e-300)
 
 
+def rel_err_heads(got, ref, H: int) -> np.ndarray:
+    """Per-(sequence, head) normwise relative error [n, H] of outputs shaped
+    [n, H, P] or [n, T, H, P]: the same metric as ``rel_err`` taken over one
+    head's elements (all drafts of a round), so that a head whose outputs are
+    small cannot hide its error behind the sequence's largest head."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    n, P = ref.shape[0], ref.shape[-1]
+    g = np.moveaxis(got.reshape(n, -1, H, P), 2, 1).reshape(n, H, -1)
+    r = np.moveaxis(ref.reshape(n, -1, H, P), 2, 1).reshape(n, H, -1)
+    return np.max(np.abs(g - r), axis=2) / np.maximum(np.max(np.abs(r), axis=2), 1e-300)
+
+
+def state_errs(t: torch.Tensor, ref: np.ndarray, idx) -> tuple[np.ndarray, np.ndarray]:
+    """Normwise relative errors of device states t fp32 [B,H,N,P] (key-major)
+    at sequences idx against the oracle's ref f64 [n,H,P,N], computed on the
+    device (full-size states): per sequence [n] and per (sequence, head) [n,H]."""
+    dev = t.device
+    g = t[torch.as_tensor(np.asarray(idx), device=dev)].to(torch.float64)
+    r = torch.from_numpy(np.ascontiguousarray(ref, dtype=np.float64)).to(dev).transpose(-1, -2)
+    d = (g - r).abs().flatten(2).amax(-1)
+    m = r.abs().flatten(2).amax(-1)
+    per_head = (d / m.clamp_min(1e-300)).cpu().numpy()
+    per_seq = (d.amax(-1) / m.amax(-1).clamp_min(1e-300)).cpu().numpy()
+    del g, r
+    return per_seq, per_head
+
+
+def parity_sample(B: int, n: int = 64, seed: int = 0) -> np.ndarray:
+    """n sequences of a batch of B for the oracle to recompute: the first, the
+    last and n - 2 others drawn without replacement (all of them if B <= n)."""
+    if B <= n:
+        return np.arange(B)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    mid = rng.choice(np.arange(1, B - 1), n - 2, replace=False)
+    return np.sort(np.concatenate([[0, B - 1], mid]))
+
+
 def state_np_to_gpu(S: np.ndarray) -> torch.Tensor:
     """[B,H,P,N] (math layout) -> device fp32 [B,H,N,P] (key-major slabs)."""
     return torch.from_numpy(np.ascontiguousarray(np.swapaxes(np.asarray(S, np.float32), -1, -2))).cuda()

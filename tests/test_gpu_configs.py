@@ -1,0 +1,147 @@
+"""Full-length GPU parity on the four serving-scale workloads, at full batch in
+the launch configuration the benchmark times.
+
+The oracle recomputes 64 sampled sequences (the first, the last and 62 drawn
+at random) over every step or round of the workload: 256 decode steps for
+the Mamba-2 and GDN layers, 128 verify + commit rounds for the two
+speculative ones.  Checked, per sequence and per (sequence, head):
+
+* every output of every step (all T drafts of a round);
+* the checkpoint after every fold, against the eager state at that point;
+* the committed state (rs_materialize) after every speculative commit, and at
+  every fifth decode step (5 is prime to L = 16, so every window position
+  h is visited);
+* the pointers and the device status word at the end.
+
+Tolerances: 2e-3 where a result comes from the fp32 checkpoint, 3e-2 where it
+is read from the bf16 one (the task's bounds for the two precisions).
+
+The two-precision GDN workload also runs the shared-bf16 arm on the same
+inputs and reports both arms' output errors (mean and max, over all rounds and
+over the rounds after each sequence's first fold): "ReplaySSM: Cache SSM
+Inputs, Not State", section "How it works", bullet "Two precisions", and the
+paper abstract.  With RS_REPORT_DIR set, the report is also written there as
+JSON.
+"""
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+import pytest
+
+from harness import (TOL_HP, TOL_LP, SpecRun, StandardRun, parity_sample, rel_err, rel_err_heads,
+                     state_errs)
+from rs_decode_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(errs: np.ndarray, tol, what: str):
+    worst = float(np.max(errs))
+    assert worst <= tol, f"{what}: rel err {worst:.3e} > {tol}"
+    return worst
+
+
+@pytest.mark.parametrize("name", ["mamba2", "gdn"])
+def test_decode_full_length(name):
+    w = synth.WORKLOADS[name]
+    idx = parity_sample(w.B)
+    run = StandardRun(w, seed=0, sample=idx)
+    folds = 0
+    for s in range(w.steps):
+        y, y_ref, folded = run.step()
+        _check(rel_err(y, y_ref), TOL_HP, f"step {s} outputs")
+        _check(rel_err_heads(y, y_ref, w.H), TOL_HP, f"step {s} outputs per head")
+        if folded:
+            folds += 1
+            per_seq, per_head = state_errs(run.layer.checkpoint_hp(), run.model.S, idx)
+            _check(per_seq, TOL_HP, f"step {s} flushed checkpoint")
+            _check(per_head, TOL_HP, f"step {s} flushed checkpoint per head")
+        if s % 5 == 4:
+            per_seq, per_head = state_errs(run.layer.materialize(), run.model.S, idx)
+            _check(per_seq, TOL_HP, f"step {s} committed state")
+            _check(per_head, TOL_HP, f"step {s} committed state per head")
+    assert folds == w.steps // w.L
+    ptr = run.layer.pointers()
+    assert (ptr["h"] == run.ptr.h).all() and (ptr["base"] == run.ptr.base).all() and (ptr["nd"] == 0).all()
+    assert run.layer.status() == 0
+
+
+def _spec_full(w, precision: str, idx):
+    """All rounds of a speculative workload; returns per-(round, sequence)
+    output errors, the fold mask and the rounds after each sequence's first
+    fold."""
+    run = SpecRun(w, seed=0, precision=precision, sample=idx)
+    n = len(idx)
+    errs = np.zeros((w.steps, n))
+    folds = np.zeros((w.steps, n), bool)
+    lp_tol = TOL_LP if precision != "fp32" else TOL_HP
+    for r in range(w.steps):
+        y, y_ref, folded, S_before, _ = run.round()
+        e = rel_err(y.reshape(n, -1), y_ref.reshape(n, -1))
+        eh = rel_err_heads(y, y_ref, w.H)
+        # two-precision: a folding sequence reads the fp32 copy; shared-bf16
+        # reads its bf16 copy in every round
+        tol = np.where(folded & (precision == "two"), TOL_HP, lp_tol)
+        assert (e <= tol).all(), f"{precision} round {r}: outputs rel err {e.max():.3e}"
+        assert (eh <= tol[:, None]).all(), f"{precision} round {r}: per-head outputs rel err {eh.max():.3e}"
+        errs[r], folds[r] = e, folded
+        if folded.any():
+            ck = run.layer.checkpoint_hp() if precision != "shared_bf16" else run.layer.checkpoint_lp_f32()
+            per_seq, per_head = state_errs(ck, S_before, idx)
+            ck_tol = TOL_LP if precision == "shared_bf16" else TOL_HP
+            _check(per_seq[folded], ck_tol, f"{precision} round {r} folded checkpoint")
+            _check(per_head[folded], ck_tol, f"{precision} round {r} folded checkpoint per head")
+        if precision != "shared_bf16":
+            per_seq, per_head = state_errs(run.layer.materialize(), run.model.S, idx)
+            _check(per_seq, TOL_HP, f"{precision} round {r} committed state")
+            _check(per_head, TOL_HP, f"{precision} round {r} committed state per head")
+    ptr = run.layer.pointers()
+    assert (ptr["h"][idx] == [run.ptrs[b].h for b in idx]).all()
+    assert (ptr["base"][idx] == [run.ptrs[b].base for b in idx]).all()
+    assert run.layer.status() == 0
+    # rounds strictly after the sequence's first fold
+    first = np.where(folds.any(0), folds.argmax(0), w.steps)
+    after = np.arange(w.steps)[:, None] > first[None, :]
+    return errs, folds, after
+
+
+def test_mamba2_spec_full_length():
+    w = synth.WORKLOADS["mamba2_spec"]
+    idx = parity_sample(w.B)
+    _, folds, _ = _spec_full(w, "fp32", idx)
+    assert folds.any(0).all(), "every sampled sequence folds at least once in 128 rounds"
+
+
+def test_gdn_spec_two_precision_full_length():
+    """Two-precision against shared-bf16 on the same inputs and sample.  Until a
+    sequence first folds, both arms read the same bf16 checkpoint values; after
+    it, the two-precision copy is a rounding of the fp32 fold while the shared
+    copy has carried bf16 rounding through every fold, so there the
+    two-precision error must not exceed the shared one."""
+    w = synth.WORKLOADS["gdn_spec"]
+    idx = parity_sample(w.B)
+    e_two, folds, after = _spec_full(w, "two", idx)
+    e_sh, folds_sh, _ = _spec_full(w, "shared_bf16", idx)
+    assert np.array_equal(folds, folds_sh)
+    assert folds.any(0).all() and after.sum() > w.steps * len(idx) // 2
+    stats = lambda e, m: {"mean": float(e[m].mean()), "max": float(e[m].max()), "n": int(m.sum())}
+    every = np.ones_like(after)
+    report = {
+        "workload": f"gdn_spec: B={w.B} H={w.H} G={w.G} P={w.P} N={w.N} L={w.L} T={w.T} capacity={w.cap} "
+                    f"accept={w.accept} rounds={w.steps}",
+        "sample": f"{len(idx)} sequences incl. 0 and {w.B - 1}",
+        "metric": "per (round, sequence) normwise relative output error vs the fp64 oracle, all T drafts",
+        "two_precision": {"all_rounds": stats(e_two, every), "after_first_fold": stats(e_two, after)},
+        "shared_bf16": {"all_rounds": stats(e_sh, every), "after_first_fold": stats(e_sh, after)},
+    }
+    print(json.dumps(report))
+    out = os.environ.get("RS_REPORT_DIR")
+    if out:
+        os.makedirs(out, exist_ok=True)
+        with open(os.path.join(out, "gdn_spec_output_error.json"), "w") as f:
+            json.dump(report, f, indent=1)
+    assert e_two[after].mean() <= e_sh[after].mean()
+    assert e_two[after].max() <= e_sh[after].max()

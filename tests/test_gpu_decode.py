@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 import torch
 
-from harness import TOL_HP, TOL_LP, StandardRun, rel_err, state_gpu_to_np, make_layer
+from harness import TOL_HP, TOL_LP, StandardRun, rel_err, rel_err_heads, state_gpu_to_np, make_layer
 from rs_decode_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -25,6 +25,8 @@ def _run_standard(w, steps, seed=0, precision="fp32", sample=None, check_materia
         # two-precision: flush steps read the fp32 copy
         tol = TOL_HP if (precision == "two" and folded) else tol_y
         assert e <= tol, f"step {s}: output rel err {e:.3e} > {tol}"
+        eh = rel_err_heads(y, y_ref, w.H).max()
+        assert eh <= tol, f"step {s}: per-head output rel err {eh:.3e} > {tol}"
         worst_y = max(worst_y, e)
         if folded:
             flushes += 1

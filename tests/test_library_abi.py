@@ -162,3 +162,33 @@ def test_oracle_does_not_reach_the_product():
             assert not re.search(r"^\s*(import|from)\s+rs_decode_gb300", src, re.M), name
             assert not re.search(r'#\s*include\s*[<"]rs', src), name
             assert "librs" not in src, name
+
+
+def test_every_declaration_cites_its_source():
+    """Each function of include/rs.h carries a "Source:" line in the comment
+    just above it (two consecutive declarations may share one): a passage of
+    the pages by its key, or "none" for plumbing with no counterpart there.
+    The keys are defined at the top of the header with the pages' titles."""
+    src = open(os.path.join(ROOT, "include", "rs.h")).read()
+    keys = {"[CSI]": "ReplaySSM: Cache SSM Inputs, Not State", "[THR]": "Songlin Yang releases ReplaySSM",
+            "[TLDR]": "ReplaySSM speeds up SSM decoding", "[ABS]": "paper abstract"}
+    head = src[:src.index("#ifndef RS_H")]
+    for key, title in keys.items():
+        assert re.search(re.escape(key) + r"\s+[\"(]?[^\n]*" + re.escape(title.split()[0]), head), key
+        assert title in re.sub(r"\s*\n\s*\*\s*", " ", head), title
+    # tokens: comments and function declarations, in order
+    toks = [(m.start(), "c", m.group(0)) for m in re.finditer(r"/\*.*?\*/", src, re.S)]
+    code = re.sub(r"/\*.*?\*/", lambda m: " " * len(m.group(0)), src, flags=re.S)
+    toks += [(m.start(), "f", m.group(1)) for m in re.finditer(r"^[a-z][\w ]*?\**\b(rs_[a-z0-9_]+)\s*\(", code, re.M)]
+    toks.sort()
+    last_comment = None
+    for _, kind, text in toks:
+        if kind == "c":
+            last_comment = text
+            continue
+        assert last_comment is not None, text
+        m = re.search(r"Source:\s*(.*)", last_comment, re.S)
+        assert m, f"{text}: no Source: line"
+        cited = m.group(1)
+        assert cited.lstrip().startswith("none") or any(k in cited for k in keys), f"{text}: {cited[:60]!r}"
+    assert sum(1 for t in toks if t[1] == "f") == len(declared_functions())
