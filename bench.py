@@ -15,9 +15,9 @@ Prints one JSON line: decode tokens/s (whole job), achieved HBM GB/s of the
 replay kernel against the measured peak, the eager load-update-store kernel
 on the same workload, an end-to-end number through host buffers, the fp64
 CPU oracle on a bounded sample, the SM clocks seen while timing, and (unless
---headline-only) the other workloads: GDN decode, Mamba-2 speculative
-verification, two-precision GDN speculative verification, each against its
-baseline kernel.
+--headline-only) the other workloads: GDN decode, decode with one decay per
+key channel, Mamba-2 speculative verification, two-precision GDN speculative
+verification, each against its baseline kernel.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 Under torchrun every rank runs its own B sequences (weak scaling, no
@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=2048)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="librs", choices=["librs", "reference"])
-    ap.add_argument("--workload", default="mamba2", choices=["mamba2", "gdn"],
+    ap.add_argument("--workload", default="mamba2", choices=["mamba2", "gdn", "kda"],
                     help="decode workload of the headline line")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -90,7 +90,7 @@ def _code_only(text: str) -> str:
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for name in ("rs_plan.cuh", "rs_replay_rows.cuh", "rs_replay_cols.cuh", "rs_replay.cu", "rs_replay_m2.cu",
-                 "rs_replay_gdn.cu", "rs_common.cuh"):
+                 "rs_replay_gdn.cu", "rs_replay_kda.cu", "rs_common.cuh"):
         with open(os.path.join(ROOT, "rs_decode_gb300", "csrc", name), encoding="utf-8") as f:
             h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
@@ -390,7 +390,8 @@ def measure_decode(w, K, W, dev, rank, world, want_eager=True, want_e2e=True, wa
             if w.kind == "mamba2":
                 rb.rs_eager_step_mamba2(desc, S_e, d["x"], d["dt"], gp["A"], d["Bm"], d["Cm"], gp["D"], y)
             else:
-                rb.rs_eager_step_gdn(desc, S_e, d["q"], d["k"], d["v"], d["alpha"], d["beta"], y)
+                fn = rb.rs_eager_step_gdn if w.kind == "gdn" else rb.rs_eager_step_kda
+                fn(desc, S_e, d["q"], d["k"], d["v"], d["alpha"], d["beta"], y)
         for s in range(W):
             eager(s)
         torch.cuda.synchronize()
@@ -620,13 +621,16 @@ def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
     peak = peak or 6800.0
     others = {}
     if not args.headline_only and world == 1 and not args.batch:
-        other = "gdn" if w.kind == "mamba2" else "mamba2"
-        g = measure_decode(synth.WORKLOADS[other], 512, W, dev, rank, world, want_e2e=False, want_clocks=False)
-        gbs = g["bytes_per_launch"] / (g["ms_per_step"] * 1e-3) / 1e9
-        others[other] = {"workload": f"{other} decode (shapes of the {other} workload), fp32 checkpoint",
-                         "value": 256 / (g["ms_per_step"] * 1e-3), "unit": "tokens/s",
-                         "ms_per_step": g["ms_per_step"], "achieved_gbs": gbs,
-                         "frac_of_measured_peak": gbs / peak, "eager": g["eager"]}
+        for other in [k for k in ("mamba2", "gdn", "kda") if k != w.kind]:
+            ow = synth.WORKLOADS[other]
+            g = measure_decode(ow, 512, W, dev, rank, world, want_e2e=False, want_clocks=False)
+            gbs = g["bytes_per_launch"] / (g["ms_per_step"] * 1e-3) / 1e9
+            others[other] = {"workload": f"{other} decode B={ow.B} H={ow.H} G={ow.G} P={ow.P} N={ow.N} L={ow.L}, "
+                                         f"fp32 checkpoint" + (", one decay per key channel" if other == "kda" else ""),
+                             "value": ow.B / (g["ms_per_step"] * 1e-3), "unit": "tokens/s",
+                             "ms_per_step": g["ms_per_step"], "achieved_gbs": gbs,
+                             "bytes_per_step": g["bytes_per_launch"], "frac_of_measured_peak": gbs / peak,
+                             "window_weighted": g["window_weighted"], "eager": g["eager"]}
         for name in ("mamba2_spec", "gdn_spec"):
             o = measure_spec(synth.WORKLOADS[name], 64, 8, dev, rank)
             o["frac_of_measured_peak"] = o["achieved_gbs"] / peak
@@ -639,7 +643,8 @@ def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
     achieved = m["bytes_per_launch"] / (m["ms_per_step"] * 1e-3) / 1e9
     clk = ClockSampler.summarise(m["clock_rows"], *m["t_wall"]) if m["clock_rows"] else None
     kernel = {"mamba2": "rows::replay_pipe_kernel<mamba2, P=64, N=128, HU=8, TMAX=1, NC=256, NS=2, SPLIT=1>",
-              "gdn": "cols::replay_pipe_kernel<gdn, P=128, N=128, TMAX=1, TC=0> (launch: HU=2, NS=5, 2 CTAs/SM)"}[w.kind]
+              "gdn": "cols::replay_pipe_kernel<gdn, P=128, N=128, TMAX=1, TC=0> (launch: HU=2, NS=5, 2 CTAs/SM)",
+              "kda": "cols::replay_pipe_kernel<kda, P=128, N=128, TMAX=1, TC=0>"}[w.kind]
     out = {
         "metric": METRIC,
         "value": w.B * K * world / (ms_total * 1e-3),

@@ -57,9 +57,10 @@
  *                        Bm, Cm [B][T][G][N] bf16, A [H] f32, D [H] f32
  *   GDN step inputs      q, k [B][T][G][N] bf16 (k-heads), v [B][T][H][P] bf16,
  *                        alpha, beta [B][T][H] f32
+ *   KDA step inputs      as GDN, but alpha [B][T][H][N] f32 (one decay per key channel)
  *   outputs              y [B][T][H][P] f32
  *   (T = 1 for the decode calls; the T axis may then be left out.)
- *   Mamba-2 head h uses B/C group h / (H/G); GDN v-head h uses k-head h / (H/G).
+ *   Mamba-2 head h uses B/C group h / (H/G); GDN (and KDA) v-head h uses k-head h / (H/G).
  */
 #ifndef RS_H
 #define RS_H
@@ -87,7 +88,11 @@ typedef enum {
 #define RS_DEV_DRAFTS_PENDING 0x4u /* decode/verify/append with uncommitted drafts; drafts dropped */
 #define RS_DEV_TIMEOUT 0x8u        /* an in-kernel wait gave up after its time limit; results invalid */
 
-typedef enum { RS_MAMBA2 = 0, RS_GDN = 1 } rs_kind;
+/* RS_KDA: Gated DeltaNet with one decay per key channel, alpha_t in R^N
+ * (a reading of Kimi Delta Attention, which [CSI] "Limits" names as
+ * compatible without defining it): D_t = S_{t-1} diag(alpha_t),
+ * u_t = beta_t (v_t - D_t k_t), S_t = D_t + u_t k_t^T, y_t = S_t q_t. */
+typedef enum { RS_MAMBA2 = 0, RS_GDN = 1, RS_KDA = 2 } rs_kind;
 
 typedef enum {
     RS_PREC_FP32 = 0,        /* fp32 checkpoint only                                          */
@@ -97,7 +102,7 @@ typedef enum {
 } rs_precision;
 
 /* Shape of one layer.  Supported (P, N): Mamba-2 (64,128), (64,64);
- * GDN (128,128), (64,64).  1 <= B <= 65535, B * H <= 2^26 (more state than
+ * GDN and KDA (128,128), (64,64); KDA with the fp32 checkpoint only.  1 <= B <= 65535, B * H <= 2^26 (more state than
  * a GPU holds; kernels index slabs with 32-bit integers), L >= 1, T_max in 0..8, and
  * max(L, T_max) + T_max <= capacity <= 32: a round of T drafts writes after
  * the h committed records it may fold, and h reaches L (or T_max, when
@@ -120,10 +125,11 @@ typedef struct {
     float *ckpt_hp;    /* fp32 checkpoint [B][H][N][P]; NULL for RS_PREC_SHARED_BF16 */
     uint16_t *ckpt_lp; /* bf16 checkpoint [B][H][N][P]; NULL for RS_PREC_FP32        */
     void *buf_v;       /* records' values: Mamba-2 x bf16 [B][cap][H][P];
-                          GDN correction term u fp32 [B][cap][H][P]                   */
+                          GDN / KDA correction term u fp32 [B][cap][H][P]             */
     uint16_t *buf_k;   /* records' keys (Mamba-2 B / GDN k) bf16 [B][cap][G][N]       */
-    float *buf_a;      /* records' decays alpha, fp32 [B][cap][H] (Mamba-2: exp(dt A))  */
-    float *buf_s;      /* Mamba-2 records' dt, fp32 [B][cap][H] (v = dt x); NULL for GDN */
+    float *buf_a;      /* records' decays alpha, fp32 [B][cap][H] (Mamba-2: exp(dt A));
+                          KDA [B][cap][H][N]                                          */
+    float *buf_s;      /* Mamba-2 records' dt, fp32 [B][cap][H] (v = dt x); NULL otherwise */
     int32_t *base;     /* [B] slot of the first record after the checkpoint          */
     int32_t *h;        /* [B] committed records after the checkpoint                 */
     int32_t *nd;       /* [B] appended, not yet accepted draft records               */
@@ -201,6 +207,18 @@ rs_status rs_decode_gdn(const rs_layer_desc *desc, const rs_state *st, const uin
                         const uint16_t *k, const uint16_t *v, const float *alpha,
                         const float *beta, float *y, void *stream);
 
+/* One decode step of a layer with per-channel decays (RS_KDA): as
+ * rs_decode_gdn, with alpha fp32 [B][H][N].  In replay form the decay
+ * weights become vectors over the key channels: y_t = S_c (gamma(t) (.) q_t)
+ * + sum_j u_j ((w_j(t) (.) k_j) . q_t), and the flush writes
+ * S_c <- S_c diag(gamma) + sum_j u_j (w_j (.) k_j)^T.  Records keep the
+ * decay vectors (fp32 [B][cap][H][N]).
+ * Source: [CSI] "Limits" (Kimi Delta Attention named as compatible but not
+ * implemented) and "How it works", Gated DeltaNet bullet. */
+rs_status rs_decode_kda(const rs_layer_desc *desc, const rs_state *st, const uint16_t *q,
+                        const uint16_t *k, const uint16_t *v, const float *alpha,
+                        const float *beta, float *y, void *stream);
+
 /* ------------------------------------------------------------------ speculative */
 /* Speculative verification of T drafts (1 <= T <= T_max), either family.
  * Appends the T draft records and writes all T outputs y [B][T][H][P] from one
@@ -265,6 +283,13 @@ rs_status rs_eager_step_mamba2(const rs_layer_desc *desc, float *S, const uint16
                                const float *dt, const float *A, const uint16_t *Bm,
                                const uint16_t *Cm, const float *D, float *y, void *stream);
 rs_status rs_eager_step_gdn(const rs_layer_desc *desc, float *S, const uint16_t *q,
+                            const uint16_t *k, const uint16_t *v, const float *alpha,
+                            const float *beta, float *y, void *stream);
+/* The eager step with per-channel decays (alpha fp32 [B][H][N]):
+ * S <- S diag(alpha) + u k^T with u = beta (v - S diag(alpha) k), y = S q.
+ * Source: [THR] post [2/N] (loading and storing the state every step); the
+ * per-channel decay as read for rs_decode_kda from [CSI] "Limits". */
+rs_status rs_eager_step_kda(const rs_layer_desc *desc, float *S, const uint16_t *q,
                             const uint16_t *k, const uint16_t *v, const float *alpha,
                             const float *beta, float *y, void *stream);
 

@@ -16,7 +16,7 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "librs.so")
 
-MAMBA2, GDN = 0, 1
+MAMBA2, GDN, KDA = 0, 1, 2
 PREC_FP32, PREC_TWO, PREC_SHARED_BF16 = 0, 1, 2
 DEV_CAPACITY, DEV_ACCEPT, DEV_DRAFTS_PENDING = 0x1, 0x2, 0x4
 STATUS = {0: "RS_OK", 1: "RS_ERR_INVALID_ARG", 2: "RS_ERR_UNSUPPORTED", 3: "RS_ERR_CAPACITY",
@@ -56,6 +56,7 @@ _SIGS = {
     "rs_get_status": [ctypes.POINTER(State), ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, _vp],
     "rs_decode_mamba2": [ctypes.POINTER(LayerDesc), ctypes.POINTER(State)] + [_vp] * 8,
     "rs_decode_gdn": [ctypes.POINTER(LayerDesc), ctypes.POINTER(State)] + [_vp] * 7,
+    "rs_decode_kda": [ctypes.POINTER(LayerDesc), ctypes.POINTER(State)] + [_vp] * 7,
     "rs_verify": [ctypes.POINTER(LayerDesc), ctypes.POINTER(State), ctypes.c_int,
                   ctypes.POINTER(Inputs), _vp, _vp],
     "rs_commit": [ctypes.POINTER(LayerDesc), ctypes.POINTER(State), _vp, _vp],
@@ -66,6 +67,7 @@ _SIGS = {
     "rs_materialize": [ctypes.POINTER(LayerDesc), ctypes.POINTER(State), _vp, _vp],
     "rs_eager_step_mamba2": [ctypes.POINTER(LayerDesc)] + [_vp] * 9,
     "rs_eager_step_gdn": [ctypes.POINTER(LayerDesc)] + [_vp] * 8,
+    "rs_eager_step_kda": [ctypes.POINTER(LayerDesc)] + [_vp] * 8,
     "rs_eager_verify_snapshots": [ctypes.POINTER(LayerDesc), _vp, _vp, ctypes.c_int,
                                   ctypes.POINTER(Inputs), _vp, _vp],
     "rs_eager_select": [ctypes.POINTER(LayerDesc), _vp, _vp, _vp, _vp],
@@ -175,6 +177,12 @@ def rs_decode_gdn(desc, state, q, k, v, alpha, beta, y, stream=None):
         _ptr(y), _stream(stream)))
 
 
+def rs_decode_kda(desc, state, q, k, v, alpha, beta, y, stream=None):
+    _check("rs_decode_kda", load().rs_decode_kda(
+        ctypes.byref(desc), ctypes.byref(state), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+        _ptr(y), _stream(stream)))
+
+
 def rs_verify(desc, state, T: int, inputs: Inputs, y, stream=None):
     _check("rs_verify", load().rs_verify(ctypes.byref(desc), ctypes.byref(state), T,
                                          ctypes.byref(inputs), _ptr(y), _stream(stream)))
@@ -211,6 +219,12 @@ def rs_eager_step_mamba2(desc, S, x, dt, A, Bm, Cm, D, y, stream=None):
 
 def rs_eager_step_gdn(desc, S, q, k, v, alpha, beta, y, stream=None):
     _check("rs_eager_step_gdn", load().rs_eager_step_gdn(
+        ctypes.byref(desc), _ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(y),
+        _stream(stream)))
+
+
+def rs_eager_step_kda(desc, S, q, k, v, alpha, beta, y, stream=None):
+    _check("rs_eager_step_kda", load().rs_eager_step_kda(
         ctypes.byref(desc), _ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(y),
         _stream(stream)))
 

@@ -27,7 +27,7 @@ namespace rs {
 
 rs_status check_desc(const rs_layer_desc *d) {
     if (!d) return RS_ERR_INVALID_ARG;
-    if (d->kind != RS_MAMBA2 && d->kind != RS_GDN) return RS_ERR_INVALID_ARG;
+    if (d->kind != RS_MAMBA2 && d->kind != RS_GDN && d->kind != RS_KDA) return RS_ERR_INVALID_ARG;
     if (d->B < 1 || d->B > 65535 || d->H < 1 || d->G < 1 || d->H % d->G != 0) return RS_ERR_INVALID_ARG;
     // kernels index slabs (sequence x head) and units with 32-bit integers; 2^26
     // slabs of the smallest shape (64 x 64 bf16) are already 512 GiB
@@ -42,6 +42,7 @@ rs_status check_desc(const rs_layer_desc *d) {
     // sequence of calls needs all of them (L + T_max when T_max <= L).
     if (d->capacity < (d->L > d->T_max ? d->L : d->T_max) + d->T_max) return RS_ERR_CAPACITY;
     if (!replay_shape_supported(d->kind, d->P, d->N)) return RS_ERR_UNSUPPORTED;
+    if (d->kind == RS_KDA && d->precision != RS_PREC_FP32) return RS_ERR_UNSUPPORTED;
     return RS_OK;
 }
 
@@ -76,8 +77,9 @@ rs_status check_inputs(int kind, const rs_inputs *in, bool need_q) {
         if (in->D && !aligned(in->D, 4)) return RS_ERR_INVALID_ARG;
         if (in->q || in->k || in->v || in->alpha || in->beta) return RS_ERR_INVALID_ARG;
     } else {
-        if (!aligned(in->q, 16) || !aligned(in->k, 16) || !aligned(in->v, 16) || !aligned(in->alpha, 4) ||
-            !aligned(in->beta, 4))
+        // KDA reads its decay vectors 16 bytes at a time
+        if (!aligned(in->q, 16) || !aligned(in->k, 16) || !aligned(in->v, 16) ||
+            !aligned(in->alpha, kind == RS_KDA ? 16 : 4) || !aligned(in->beta, 4))
             return RS_ERR_INVALID_ARG;
         if (in->x || in->dt || in->A || in->Bm || in->Cm || in->D) return RS_ERR_INVALID_ARG;
     }
@@ -139,7 +141,7 @@ rs_status rs_state_bytes_for(const rs_layer_desc *d, rs_state_bytes *o) {
     o->ckpt_lp = d->precision != RS_PREC_FP32 ? B * H * N * P * 2 : 0;
     o->buf_v = B * C * H * P * (d->kind == RS_MAMBA2 ? 2 : 4);
     o->buf_k = B * C * G * N * 2;
-    o->buf_a = B * C * H * 4;
+    o->buf_a = B * C * H * (d->kind == RS_KDA ? N : 1) * 4;
     o->buf_s = d->kind == RS_MAMBA2 ? B * C * H * 4 : 0;
     o->base = o->h = o->nd = o->arrive = B * 4;
     o->status = 4;
@@ -191,6 +193,21 @@ rs_status rs_decode_gdn(const rs_layer_desc *d, const rs_state *st, const uint16
     rs_inputs in = {};
     in.q = q; in.k = k; in.v = v; in.alpha = alpha; in.beta = beta;
     RS_TRY(check_inputs(RS_GDN, &in, true));
+    if (!aligned(y, 16)) return RS_ERR_INVALID_ARG;
+    ReplayParams p = replay_params(d, st, MODE_DECODE, 1);
+    set_inputs(p, in);
+    p.y = y;
+    return cuda_status(replay_launch(p, d->kind, d->P, d->N, (cudaStream_t)stream));
+}
+
+rs_status rs_decode_kda(const rs_layer_desc *d, const rs_state *st, const uint16_t *q, const uint16_t *k,
+                        const uint16_t *v, const float *alpha, const float *beta, float *y, void *stream) {
+    RS_TRY(check_desc(d));
+    if (d->kind != RS_KDA) return RS_ERR_INVALID_ARG;
+    RS_TRY(check_state(d, st));
+    rs_inputs in = {};
+    in.q = q; in.k = k; in.v = v; in.alpha = alpha; in.beta = beta;
+    RS_TRY(check_inputs(RS_KDA, &in, true));
     if (!aligned(y, 16)) return RS_ERR_INVALID_ARG;
     ReplayParams p = replay_params(d, st, MODE_DECODE, 1);
     set_inputs(p, in);
@@ -272,6 +289,20 @@ rs_status rs_eager_step_gdn(const rs_layer_desc *d, float *S, const uint16_t *q,
     rs_inputs in = {};
     in.q = q; in.k = k; in.v = v; in.alpha = alpha; in.beta = beta;
     RS_TRY(check_inputs(RS_GDN, &in, true));
+    EagerParams p = {};
+    p.B = d->B; p.H = d->H; p.G = d->G; p.T = 1; p.slots = 1; p.S = S;
+    p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta; p.y = y;
+    return cuda_status(eager_launch(p, d->kind, d->P, d->N, (cudaStream_t)stream));
+}
+
+rs_status rs_eager_step_kda(const rs_layer_desc *d, float *S, const uint16_t *q, const uint16_t *k,
+                            const uint16_t *v, const float *alpha, const float *beta, float *y, void *stream) {
+    RS_TRY(check_desc(d));
+    if (d->kind != RS_KDA) return RS_ERR_INVALID_ARG;
+    if (!aligned(S, 16) || !aligned(y, 16)) return RS_ERR_INVALID_ARG;
+    rs_inputs in = {};
+    in.q = q; in.k = k; in.v = v; in.alpha = alpha; in.beta = beta;
+    RS_TRY(check_inputs(RS_KDA, &in, true));
     EagerParams p = {};
     p.B = d->B; p.H = d->H; p.G = d->G; p.T = 1; p.slots = 1; p.S = S;
     p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta; p.y = y;

@@ -11,6 +11,8 @@
 //   Mamba-2: S <- alpha S + (dt x) k^T, y = S q + D x  (row-local update)
 //   GDN:     a = S k, u = beta (v - alpha a), S <- alpha S + u k^T,
 //            y = S_new q = alpha (S q) + u (k . q)
+//   KDA (one decay per key channel): a = S (alpha (.) k), u = beta (v - a),
+//            S <- S diag(alpha) + u k^T, y = S (alpha (.) q) + u (k . q)
 #include "rs_common.cuh"
 #include "rs_internal.h"
 
@@ -20,7 +22,8 @@ template <int KIND, int P, int N, int HPC, int NT>
 __global__ void __launch_bounds__(NT) eager_kernel(const EagerParams p) {
     using Gm = Geo<P, N, NT, float>;
     constexpr int VEC = Gm::VEC, TPR = Gm::TPR, R = Gm::R;
-    constexpr int J1 = KIND == RS_GDN ? 2 : 1;
+    constexpr bool KDA = KIND == RS_KDA;
+    constexpr int J1 = KIND != RS_MAMBA2 ? 2 : 1;
     extern __shared__ __align__(16) float sm[];
     float *kq = sm;                              // [2*kMaxT][N]: k_i rows 0.., q_i rows kMaxT..
     float *vv = kq + 2 * kMaxT * N;              // [HPC][kMaxT][P]: Mamba-2 dt*x, GDN v
@@ -28,6 +31,7 @@ __global__ void __launch_bounds__(NT) eager_kernel(const EagerParams p) {
     float *kqd = sc + HPC * kMaxT * 2;           // [kMaxT] k_i . q_i (GDN)
     float *uu = kqd + kMaxT;                     // [HPC][P] GDN u of the current draft
     float *red = uu + HPC * P;                   // [NW][HPC*J1][P]
+    float *av = red + (NT / 32) * HPC * J1 * P;  // KDA: [HPC][kMaxT][N] decay vectors
 
     const int tid = threadIdx.x;
     const int b = blockIdx.y, h0 = blockIdx.x * HPC;
@@ -61,18 +65,24 @@ __global__ void __launch_bounds__(NT) eager_kernel(const EagerParams p) {
         const float xv = bf2f(src[bti * P + pp]);
         vv[(hd * kMaxT + i) * P + pp] = KIND == RS_MAMBA2 ? p.dt[bti] * xv : xv;
     }
+    if (KDA) {
+        for (int it = tid; it < HPC * T * N; it += NT) {
+            const int n = it % N, i = (it / N) % T, hd = it / (N * T), hh = h0 + hd;
+            av[((size_t)hd * kMaxT + i) * N + n] = p.alpha[(((size_t)b * T + i) * H + hh) * N + n];
+        }
+    }
     for (int it = tid; it < HPC * T; it += NT) {
         const int i = it % T, hd = it / T, hh = h0 + hd;
         const size_t bti = ((size_t)b * T + i) * H + hh;
         if (KIND == RS_MAMBA2) {
             sc[(hd * kMaxT + i) * 2] = expf(p.dt[bti] * p.A[hh]);
         } else {
-            sc[(hd * kMaxT + i) * 2] = p.alpha[bti];
+            sc[(hd * kMaxT + i) * 2] = KDA ? 1.f : p.alpha[bti];
             sc[(hd * kMaxT + i) * 2 + 1] = p.beta[bti];
         }
     }
     __syncthreads();
-    if (KIND == RS_GDN) {  // k_i . q_i, one warp per draft
+    if (KIND != RS_MAMBA2) {  // k_i . q_i, one warp per draft
         const int w = tid / 32, lane = tid % 32;
         for (int i = w; i < T; i += NT / 32) {
             float a = 0.f;
@@ -127,7 +137,9 @@ __global__ void __launch_bounds__(NT) eager_kernel(const EagerParams p) {
                 for (int k = 0; k < R; ++k) {
                     float s[VEC];
                     unpack<float, VEC>(tile[hd][k], s);
-                    const float kn = kvec[k], qn = qvec[k];
+                    // KDA: S diag(alpha) k and S diag(alpha) q
+                    const float an = KDA ? av[((size_t)hd * kMaxT + i) * N + n0 + k] : 1.f;
+                    const float kn = kvec[k] * an, qn = qvec[k] * an;
 #pragma unroll
                     for (int e = 0; e < VEC; ++e) {
                         acc[hd * 2][e] = fmaf(s[e], kn, acc[hd * 2][e]);
@@ -155,8 +167,9 @@ __global__ void __launch_bounds__(NT) eager_kernel(const EagerParams p) {
                     float s[VEC];
                     unpack<float, VEC>(tile[hd][k], s);
                     const float kn = kvec[k];
+                    const float ar = KDA ? av[((size_t)hd * kMaxT + i) * N + n0 + k] : al;  // this row's decay
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) s[e] = fmaf(al, s[e], uloc[e] * kn);
+                    for (int e = 0; e < VEC; ++e) s[e] = fmaf(ar, s[e], uloc[e] * kn);
                     tile[hd][k] = make_uint4(__float_as_uint(s[0]), __float_as_uint(s[1]),
                                              __float_as_uint(s[2]), __float_as_uint(s[3]));
                 }
@@ -176,9 +189,9 @@ __global__ void __launch_bounds__(NT) eager_kernel(const EagerParams p) {
 
 template <int KIND, int P, int N, int HPC, int NT>
 static cudaError_t launch_eager(const EagerParams &p, cudaStream_t s) {
-    constexpr int J1 = KIND == RS_GDN ? 2 : 1;
+    constexpr int J1 = KIND != RS_MAMBA2 ? 2 : 1;
     const size_t floats = 2 * kMaxT * N + HPC * kMaxT * P + HPC * kMaxT * 2 + kMaxT + HPC * P +
-                          (NT / 32) * HPC * J1 * P;
+                          (NT / 32) * HPC * J1 * P + (KIND == RS_KDA ? HPC * kMaxT * N : 0);
     const size_t smem = floats * sizeof(float);
     auto kern = eager_kernel<KIND, P, N, HPC, NT>;
     static SmemGrants grants;  // this instantiation's opt-in, per device
@@ -195,9 +208,12 @@ cudaError_t eager_launch(const EagerParams &p, int kind, int P, int N, cudaStrea
                                             : launch_eager<RS_MAMBA2, 64, 128, 1, 256>(p, s);
         if (P == 64 && N == 64) return two ? launch_eager<RS_MAMBA2, 64, 64, 2, 128>(p, s)
                                            : launch_eager<RS_MAMBA2, 64, 64, 1, 128>(p, s);
-    } else {
+    } else if (kind == RS_GDN) {
         if (P == 128 && N == 128) return launch_eager<RS_GDN, 128, 128, 1, 256>(p, s);
         if (P == 64 && N == 64) return launch_eager<RS_GDN, 64, 64, 1, 128>(p, s);
+    } else {
+        if (P == 128 && N == 128) return launch_eager<RS_KDA, 128, 128, 1, 256>(p, s);
+        if (P == 64 && N == 64) return launch_eager<RS_KDA, 64, 64, 1, 128>(p, s);
     }
     return cudaErrorInvalidValue;
 }

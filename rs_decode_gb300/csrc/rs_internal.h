@@ -90,6 +90,7 @@ cudaError_t replay_launch(const ReplayParams &p, int kind, int P, int N, cudaStr
 // Per family / slab shape (one translation unit each, compiled in parallel).
 cudaError_t replay_launch_m2_64x128(const ReplayParams &p, cudaStream_t s);
 cudaError_t replay_launch_gdn_128x128(const ReplayParams &p, cudaStream_t s);
+cudaError_t replay_launch_kda_128x128(const ReplayParams &p, cudaStream_t s);
 cudaError_t replay_launch_64x64(const ReplayParams &p, int kind, cudaStream_t s);
 cudaError_t eager_launch(const EagerParams &p, int kind, int P, int N, cudaStream_t s);
 

@@ -102,12 +102,14 @@ cudaError_t replay_launch_64x64(const ReplayParams &p, int kind, cudaStream_t s)
         if (T > 1) return rows::launch_shape<RS_MAMBA2, 64, 64, 128, 4, 1, 2, 1>(p, s);
         return rows::launch_shape<RS_MAMBA2, 64, 64, 128, 1, 1, 2, 1>(p, s);
     }
+    if (kind == RS_KDA) return cols::dispatch_shape<RS_KDA, 64, 64>(p, s);
     return cols::dispatch_shape<RS_GDN, 64, 64>(p, s);
 }
 
 cudaError_t replay_launch(const ReplayParams &p, int kind, int P, int N, cudaStream_t s) {
     if (kind == RS_MAMBA2 && P == 64 && N == 128) return replay_launch_m2_64x128(p, s);
     if (kind == RS_GDN && P == 128 && N == 128) return replay_launch_gdn_128x128(p, s);
+    if (kind == RS_KDA && P == 128 && N == 128) return replay_launch_kda_128x128(p, s);
     if (P == 64 && N == 64) return replay_launch_64x64(p, kind, s);
     return cudaErrorInvalidValue;
 }

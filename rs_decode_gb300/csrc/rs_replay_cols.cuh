@@ -43,6 +43,13 @@
 // so no second launch is needed.  Every wait is bounded: on a time-out the CTA
 // raises RS_DEV_TIMEOUT, drains its copies and returns.
 //
+// Per-channel decay (RS_KDA, a reading of Kimi Delta Attention: GDN with one
+// decay per key channel) runs the GDN structure with three changes: the prep
+// warps form per-channel suffix products of the decays in one reverse scan per
+// head and fold them into the record dots and the fold keys; the dot vectors
+// are per head, gamma (.) k and gamma (.) q, so the consumers' dots need no
+// decay factor; and the fold scales each key row n of the slab by gamma[n].
+//
 // Two instantiations per shape.  TC = false: CUDA cores only, two CTAs per SM.
 // TC = true (two-precision GDN launches): the bf16 blocks are dotted with the
 // draft vectors on the tensor cores (tcgen05.mma, accumulator in TMEM).  A
@@ -64,14 +71,17 @@ namespace cols {
 template <int KIND_, int P_, int N_, int TMAX_>
 struct RCfg {
     static constexpr int KIND = KIND_, P = P_, N = N_, TMAX = TMAX_;
+    static constexpr bool DELTA = KIND != RS_MAMBA2;    // records hold the correction u (GDN, KDA)
+    static constexpr bool KDA = KIND == RS_KDA;          // one decay per key channel
     static constexpr int NCW = 4;                         // consumer warps (warps 0..NCW-1)
     static constexpr int NPW = 3;                         // prep warps (after the producer warp)
     static constexpr int NT = 32 * (NCW + 1 + NPW);       // + the producer warp (warp NCW)
     static constexpr int PREP0 = 32 * (NCW + 1);          // first prep thread
     static constexpr int NPT = 32 * NPW;                  // prep threads
     // vectors dotted with every slab: Mamba-2 the queries C_i; GDN the keys
-    // k_{m_i} (slots 0..TMAX-1) and the queries q_i (slots TMAX..2TMAX-1)
-    static constexpr int JP = (KIND == RS_GDN ? 2 : 1) * TMAX;
+    // k_{m_i} (slots 0..TMAX-1) and the queries q_i (slots TMAX..2TMAX-1);
+    // KDA the same scaled per head by the channels' decay products
+    static constexpr int JP = (DELTA ? 2 : 1) * TMAX;
     static constexpr int STAGE = N * 128;                 // one row block: N lines of 128 bytes
     static constexpr int QW = JP % 4 == 0 ? 4 : (JP % 2 == 0 ? 2 : 1);  // query floats per shared-memory vector
     static constexpr int QC = JP / QW;                    // vectors per key row
@@ -80,7 +90,7 @@ struct RCfg {
     template <int VEC> static constexpr int jn() { return VEC * JP <= 64 ? JP : 64 / VEC; }
     static_assert(N % 8 == 0 && N <= 256, "a stage is one tensor box");
     // the Mamba-2 output reduction halves down to single sums: a power-of-two bucket
-    static_assert(KIND == RS_GDN || (JP & (JP - 1)) == 0, "draft bucket");
+    static_assert(DELTA || (JP & (JP - 1)) == 0, "draft bucket");
     static constexpr int JPP = JP <= 1 ? 1 : 2 << ilog2(JP - 1);  // JP rounded up to a power of two
     // bf16 row blocks of GDN heads (P = 128: both blocks of a head form one
     // M = 128 operand) are dotted on the tensor cores: D[P x 16] = S_c^T-view x
@@ -150,7 +160,7 @@ struct UnitHdr {
 // the u of the launch's own records, written and read by the same warp.
 struct RSmem {
     int stages, bars, plans, abort, tmem, d1, d2, sr, cst, fcf, unew, ctx0, ctx_bytes;
-    int hdr, kraw, ar, vb, bt, c1, c2, g1, g2, fw, gF, pre1, pre2, qs;  // within a context
+    int hdr, kraw, ar, vb, bt, c1, c2, g1, g2, fw, gF, pre1, pre2, qs, gv, fk;  // within a context
     int total;
 };
 
@@ -166,7 +176,7 @@ __host__ __device__ inline int fold_chunk(int cap) { return cap <= 24 ? 16 : 8; 
 template <class C>
 __host__ __device__ inline RSmem replay_smem(int cap, int HU, int NS) {
     constexpr int TMAX = C::TMAX, P = C::P, N = C::N;
-    constexpr bool GDN = C::KIND == RS_GDN;
+    constexpr bool GDN = C::DELTA, KDA = C::KDA;  // (GDN: either delta-rule family)
     RSmem s;
     int o = 0;
     s.stages = o; o += NS * C::STAGE;
@@ -174,8 +184,8 @@ __host__ __device__ inline RSmem replay_smem(int cap, int HU, int NS) {
     s.plans = o;  o += al16(kPlanRing * (int)sizeof(UnitHdr));
     s.abort = o;  o += 16;
     s.tmem = o;   o += 16;                                          // TMEM address of the D buffers
-    s.d1 = o;     o += al16(cap * TMAX * 4);                        // k_r . q_i (GDN: k_r . k_{m_i})
-    s.d2 = o;     o += GDN ? al16(cap * TMAX * 4) : 0;              // GDN k_r . q_i
+    s.d1 = o;     o += KDA ? 0 : al16(cap * TMAX * 4);              // k_r . q_i (GDN: k_r . k_{m_i})
+    s.d2 = o;     o += GDN && !KDA ? al16(cap * TMAX * 4) : 0;      // GDN k_r . q_i
     s.sr = o;     o += al16(HU * cap * 4);                          // Mamba-2 dt_r
     s.cst = o;    o += al16(2 * HU * 4);                            // Mamba-2 A_h, D_h
     s.fcf = o;    o += al16(fold_chunk(cap) * P * 4);               // consumer warps' fold coefficients
@@ -185,7 +195,7 @@ __host__ __device__ inline RSmem replay_smem(int cap, int HU, int NS) {
     int c = 0;
     s.hdr = c;    c += al16((int)sizeof(UnitHdr));
     s.kraw = c;   c += al16((cap + TMAX) * N * 2);                  // bf16 keys (rows < cap), queries (cap + i)
-    s.ar = c;     c += al16(HU * cap * 4);                          // decays alpha_r
+    s.ar = c;     c += KDA ? 0 : al16(HU * cap * 4);                // decays alpha_r (KDA: read in the scan)
     s.vb = c;     c += GDN ? al16(TMAX * HU * P * 2) : 0;           // GDN drafts' v (bf16)
     s.bt = c;     c += GDN ? al16(TMAX * HU * 4) : 0;               // GDN drafts' beta
     s.c1 = c;     c += al16(HU * TMAX * cap * 4);
@@ -196,8 +206,13 @@ __host__ __device__ inline RSmem replay_smem(int cap, int HU, int NS) {
     s.gF = c;     c += al16(HU * 4);
     s.pre1 = c;   c += al16(HU * TMAX * P * 4);                     // record parts of the outputs
     s.pre2 = c;   c += GDN ? al16(HU * TMAX * P * 4) : 0;
-    // fp32 dot vectors [QC][N][QW], or (tensor-core units) the bf16 B operand
-    s.qs = c;     c += al16(C::UMMA && C::QB_BYTES > N * C::JP * 4 ? C::QB_BYTES : N * C::JP * 4);
+    // fp32 dot vectors [QC][N][QW] (KDA: one set per head), or (tensor-core
+    // units) the bf16 B operand
+    s.qs = c;     c += al16(KDA ? HU * N * C::JP * 4 : (C::UMMA && C::QB_BYTES > N * C::JP * 4 ? C::QB_BYTES : N * C::JP * 4));
+    // KDA fold: gamma(F-1) per key channel [HU][N], the decayed keys
+    // w_r(F-1) (.) k_r of the folded records [HU][cap][N], fp32
+    s.gv = c;     c += KDA ? al16(HU * N * 4) : 0;
+    s.fk = c;     c += KDA ? al16(HU * cap * N * 4) : 0;
     s.ctx_bytes = c;
     s.ctx0 = o;   o += 2 * c;
     s.total = o;
@@ -445,20 +460,31 @@ __device__ __forceinline__ void gather_fold_coefs(float *cfs, const FoldSrc &fs,
     __syncwarp();
 }
 
+// The fold's factor of key row n: gF for one decay per head; gamma(F-1)[n]
+// (gvh, the head's per-channel products) for KDA.
+template <class C>
+__device__ __forceinline__ float fold_row_scale(const float *gvh, float gf, int n) {
+    if constexpr (C::KDA) return gvh[n];
+    else return gf;
+}
+
 // Adds records r0 .. r0+nr-1 of the fold S_new = gF S_c + sum_r (fw_r v_r) k_r^T
 // to the lane's RK rows (row0, row0 + RGW, ...) of one row block: o[k][e].
+// KDA: the keys are the head's fp32 decayed keys fkh [cap][N] (w_r (.) k_r).
 template <class C, typename TE>
 __device__ __forceinline__ void fold_records(float (&o)[WGeo<C, TE>::RK][WGeo<C, TE>::VEC], const uint16_t *kraw,
-                                             const float *cfs, int lcol, int r0, int nr, int row0) {
+                                             const float *fkh, const float *cfs, int lcol, int r0, int nr,
+                                             int row0) {
     using W = WGeo<C, TE>;
     constexpr int VEC = W::VEC, RK = W::RK, RGW = W::RGW, N = C::N, WC = C::P / C::NCW;
     for (int r = 0; r < nr; ++r) {
         float cf[VEC];
         load_f32_vec<VEC>(cfs + r * WC + lcol, cf);
         const uint16_t *kr = kraw + (size_t)(r0 + r) * N + row0;
+        const float *fr = C::KDA ? fkh + (size_t)(r0 + r) * N + row0 : nullptr;
 #pragma unroll
         for (int k = 0; k < RK; ++k) {
-            const float kv = bf2f(kr[k * RGW]);
+            const float kv = C::KDA ? fr[k * RGW] : bf2f(kr[k * RGW]);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) o[k][e] = fmaf(cf[e], kv, o[k][e]);
         }
@@ -512,7 +538,8 @@ __device__ __forceinline__ void release_stage(uint64_t *empty, Ring q) {
     if ((threadIdx.x & 31) == 0) mbar_arrive(empty + q.s);
 }
 
-// Fold of the lane's columns of a head whose NCB row blocks are all staged.
+// Fold of the lane's columns of a head whose NCB row blocks are all staged
+// (KDA: gvh and fkh are the head's per-channel products and decayed keys).
 // Coefficients are gathered fc records at a time.  fp32 blocks keep the
 // partial sums in place between chunks (each lane rewrites only its own
 // elements), so each chunk is gathered once per head; bf16 blocks (shared-bf16
@@ -522,9 +549,9 @@ __device__ __forceinline__ void release_stage(uint64_t *empty, Ring q) {
 template <class C, typename TE>
 __device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages, int lane_off, Ring q0, int NS,
                                           uint64_t *empty, const uint16_t *kraw,
-                                          float *cfs, const FoldSrc &fs, const float *fw, float gf, int F, int j,
-                                          int row0, int col0, int wcol0, int lcol, size_t goff, bool materialize,
-                                          int lane, int fc) {
+                                          float *cfs, const FoldSrc &fs, const float *fw, float gf, const float *gvh,
+                                          const float *fkh, int F, int j, int row0, int col0, int wcol0, int lcol,
+                                          size_t goff, bool materialize, int lane, int fc) {
     using W = WGeo<C, TE>;
     constexpr int VEC = W::VEC, RK = W::RK, RGW = W::RGW, NCB = W::NCB, RB = W::RB;
     constexpr size_t RSTEP = (size_t)RGW * NCB * 128;
@@ -546,15 +573,17 @@ __device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages
                 for (int k = 0; k < 8; ++k) {
                     const int line = (8 * rg + k) * NCB + cb;
                     unpack<float, 4>(ld_u4(sb + line * 128 + ((cg ^ (line & 7)) << 4)), o[k]);
+                    const float sc = fold_row_scale<C>(gvh, gf, rb * RB + 8 * rg + k);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) o[k][e] *= gf;
+                    for (int e = 0; e < 4; ++e) o[k][e] *= sc;
                 }
                 release_stage(empty, ring_add(q0, rb, NS));  // the block is in registers
                 const uint16_t *kr = kraw + rb * RB + 8 * rg;
                 for (int r = 0; r < F; ++r) {
                     float cf[4], kv[8];
                     load_f32_vec<4>(cfs + r * (C::P / C::NCW) + lcol, cf);
-                    unpack<uint16_t, 8>(ld_u4(kr + (size_t)r * C::N), kv);
+                    if constexpr (C::KDA) load_f32_vec<8>(fkh + (size_t)r * C::N + rb * RB + 8 * rg, kv);
+                    else unpack<uint16_t, 8>(ld_u4(kr + (size_t)r * C::N), kv);
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
 #pragma unroll
@@ -583,9 +612,11 @@ __device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages
 #pragma unroll
                 for (int k = 0; k < RK; ++k) {
                     unpack<TE, VEC>(ld_u4(blk(rb) + k * RSTEP), o[k]);
-                    if (c == 0)
+                    if (c == 0) {
+                        const float sc = fold_row_scale<C>(gvh, gf, rb * RB + row0 + k * RGW);
 #pragma unroll
-                        for (int e = 0; e < VEC; ++e) o[k][e] *= gf;
+                        for (int e = 0; e < VEC; ++e) o[k][e] *= sc;
+                    }
                 }
                 if (c == nch - 1) {
                     // the block is in registers; partial sums written into the
@@ -593,7 +624,7 @@ __device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages
                     if (nch > 1) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     release_stage(empty, ring_add(q0, rb, NS));
                 }
-                fold_records<C, TE>(o, kraw, cfs, lcol, r0, nr > 0 ? nr : 0, rb * RB + row0);
+                fold_records<C, TE>(o, kraw, fkh, cfs, lcol, r0, nr > 0 ? nr : 0, rb * RB + row0);
                 if (c == nch - 1) {
                     fold_store<C, TE>(p, o, rb * RB + row0, col0, goff, materialize);
                 } else {
@@ -609,14 +640,15 @@ __device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages
 #pragma unroll
             for (int k = 0; k < RK; ++k) {
                 unpack<TE, VEC>(ld_u4(blk(rb) + k * RSTEP), o[k]);
+                const float sc = fold_row_scale<C>(gvh, gf, rb * RB + row0 + k * RGW);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) o[k][e] *= gf;
+                for (int e = 0; e < VEC; ++e) o[k][e] *= sc;
             }
             release_stage(empty, ring_add(q0, rb, NS));  // the block is in registers
             for (int c = 0; c < nch; ++c) {
                 const int r0 = c * fc, nr = F - r0 < fc ? F - r0 : fc;
                 gather_fold_coefs<C>(cfs, fs, fw, r0, nr > 0 ? nr : 0, j, wcol0, lane);
-                fold_records<C, TE>(o, kraw, cfs, lcol, r0, nr > 0 ? nr : 0, rb * RB + row0);
+                fold_records<C, TE>(o, kraw, fkh, cfs, lcol, r0, nr > 0 ? nr : 0, rb * RB + row0);
             }
             fold_store<C, TE>(p, o, rb * RB + row0, col0, goff, materialize);
         }
@@ -643,6 +675,124 @@ __device__ __forceinline__ bool head_pass(float (&acc)[WGeo<C, TE>::M], const Re
         if (!hold) release_stage(empty, q);
     }
     return ok;
+}
+
+// ---------------------------------------------------------------------------
+// KDA: the per-channel decay products of one unit, one warp per head and lane
+// = key channels lane + 32 t.  With w_r(m) = prod_{s=r+1..m} alpha_s and
+// gamma(m) = prod_{s<=m} alpha_s, both vectors over the key channels, the
+// state after record m is S_m = S_c diag(gamma(m)) + sum_{r<=m} u_r
+// (w_r(m) (.) k_r)^T, so for draft i at position m_i = hc + i:
+//   S_{m_i - 1} diag(alpha_{m_i}) k_{m_i} = S_c (gamma(m_i) (.) k_{m_i})
+//                                        + sum_{r<m_i} u_r ((w_r(m_i) (.) k_r) . k_{m_i})
+//   y_i = S_{m_i} q_i = S_c (gamma(m_i) (.) q_i) + sum_{r<=m_i} u_r ((w_r(m_i) (.) k_r) . q_i)
+// One reverse pass over the records keeps a running product per bound (the
+// drafts' m_i and the fold's F-1) and writes
+//   c1[i][r] = (w_r(m_i) (.) k_r) . k_{m_i} (r < m_i),  c2[i][r] = (w_r(m_i) (.) k_r) . q_i (r <= m_i),
+//   the fold keys fk[r] = w_r(F-1) (.) k_r (r < F) and gv = gamma(F-1),
+//   the head's dot vectors gamma(m_i) (.) k_{m_i} and gamma(m_i) (.) q_i,
+// and the GDN factors it replaces as ones (g1 = g2 = fw = gF = 1), so that the
+// consumers' recurrence u_i = beta_i (v_i - sk_i) and outputs follow unchanged.
+template <class C>
+__device__ __forceinline__ bool kda_scan(const ReplayParams &p, uint8_t *cx, const RSmem &L, const SeqPlan &s,
+                                         const int b, const int h0, const int HU, const PipeCtx &pc) {
+    constexpr int N = C::N, TMAX = C::TMAX, JP = C::JP, JPP = C::JPP, QW = C::QW;
+    constexpr int NPL = N / 32, LJ = ilog2(JPP);
+    static_assert(N % 32 == 0, "key channels per lane");
+    const int tp = pc.tid - C::PREP0, lane = tp & 31, pw = tp >> 5;
+    const int H = p.H, cap = p.cap;
+    const int base = s.base, hc = s.hc, T = s.T;
+    const int nrec = hc + T;
+    // the fold's records: F - 1 is the last folded position
+    const int F = (s.fold || p.mode == MODE_MATERIALIZE) ? s.F : 0;
+    auto slot = [&](int r) {
+        const int v = base + r;
+        return v >= cap ? v - cap : v;
+    };
+    const uint16_t *kraw = reinterpret_cast<const uint16_t *>(cx + L.kraw);
+    float *c1 = reinterpret_cast<float *>(cx + L.c1), *c2 = reinterpret_cast<float *>(cx + L.c2);
+    float *g1 = reinterpret_cast<float *>(cx + L.g1), *g2 = reinterpret_cast<float *>(cx + L.g2);
+    float *fw = reinterpret_cast<float *>(cx + L.fw), *gF = reinterpret_cast<float *>(cx + L.gF);
+    float *qs = reinterpret_cast<float *>(cx + L.qs);
+    float *gv = reinterpret_cast<float *>(cx + L.gv), *fk = reinterpret_cast<float *>(cx + L.fk);
+    for (int hd = pw; hd < HU; hd += C::NPW) {
+        const int hh = h0 + hd;
+        float Pd[TMAX][NPL], PF[NPL];  // running products: prod_{s=r+1..m} alpha_s[n]
+#pragma unroll
+        for (int t = 0; t < NPL; ++t) {
+            PF[t] = 1.f;
+#pragma unroll
+            for (int i = 0; i < TMAX; ++i) Pd[i][t] = 1.f;
+        }
+        for (int r = nrec - 1; r >= 0; --r) {
+            const float *asrc = r < hc ? p.buf_a + (((size_t)b * cap + slot(r)) * H + hh) * N
+                                       : p.alpha + (((size_t)b * T + (r - hc)) * H + hh) * N;
+            float a[NPL], kr[NPL];
+#pragma unroll
+            for (int t = 0; t < NPL; ++t) {
+                a[t] = asrc[lane + 32 * t];
+                kr[t] = bf2f(kraw[(size_t)r * N + lane + 32 * t]);
+            }
+            if (T > 0) {
+                // slots i < TMAX: (w (.) k_r) . k_{m_i}; TMAX + i: (w (.) k_r) . q_i
+                float v[JPP];
+#pragma unroll
+                for (int jj = 0; jj < JPP; ++jj) v[jj] = 0.f;
+#pragma unroll
+                for (int i = 0; i < TMAX; ++i) {
+                    if (i < T && r <= hc + i) {
+#pragma unroll
+                        for (int t = 0; t < NPL; ++t) {
+                            const int n = lane + 32 * t;
+                            const float wk = Pd[i][t] * kr[t];
+                            v[i] = fmaf(wk, bf2f(kraw[(size_t)(hc + i) * N + n]), v[i]);
+                            v[TMAX + i] = fmaf(wk, bf2f(kraw[(size_t)(cap + i) * N + n]), v[TMAX + i]);
+                        }
+                    }
+                }
+                RowReduce<JPP, JPP, 1, 16, 0>::run(v, lane);
+                const int sh = 5 - LJ;
+                if ((lane & ((1 << sh) - 1)) == 0) {
+                    const int jj = lane >> sh;
+                    if (jj < TMAX) {
+                        if (jj < T) c1[(hd * TMAX + jj) * cap + r] = r < hc + jj ? v[0] : 0.f;
+                    } else if (jj < JP && jj - TMAX < T) {
+                        const int i = jj - TMAX;
+                        c2[(hd * TMAX + i) * cap + r] = r <= hc + i ? v[0] : 0.f;
+                    }
+                }
+            }
+            if (r < F) {
+#pragma unroll
+                for (int t = 0; t < NPL; ++t) fk[((size_t)hd * cap + r) * N + lane + 32 * t] = PF[t] * kr[t];
+            }
+#pragma unroll
+            for (int t = 0; t < NPL; ++t) {
+#pragma unroll
+                for (int i = 0; i < TMAX; ++i)
+                    if (i < T && r <= hc + i) Pd[i][t] *= a[t];
+                if (r < F) PF[t] *= a[t];
+            }
+        }
+        // the running products are now gamma(m_i) and gamma(F - 1)
+        float *qh = qs + (size_t)hd * N * JP;
+#pragma unroll
+        for (int t = 0; t < NPL; ++t) {
+            const int n = lane + 32 * t;
+#pragma unroll
+            for (int jj = 0; jj < JP; ++jj) {
+                const int i = jj < TMAX ? jj : jj - TMAX;
+                const int row = i < T ? (jj < TMAX ? hc + i : cap + i) : -1;
+                qh[((size_t)(jj / QW) * N + n) * QW + jj % QW] =
+                    row >= 0 ? Pd[i][t] * bf2f(kraw[(size_t)row * N + n]) : 0.f;
+            }
+            gv[(size_t)hd * N + n] = F > 0 ? PF[t] : 1.f;
+        }
+        if (lane < TMAX) g1[hd * TMAX + lane] = g2[hd * TMAX + lane] = 1.f;
+        if (lane < F) fw[hd * cap + lane] = 1.f;
+        if (lane == 0) gF[hd] = 1.f;
+    }
+    return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -699,7 +849,7 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
     auto u_src = [&](int task, int r) {
         return ubuf + (((size_t)b * cap + slot(r)) * H + h0 + task / PC4) * P + 4 * (task % PC4);
     };
-    const bool u_pre = KIND == RS_GDN && T > 0 && tp < HU * PC4;
+    const bool u_pre = C::DELTA && T > 0 && tp < HU * PC4;
     float4 uv[8];
 #pragma unroll
     for (int t = 0; t < 8; ++t)
@@ -738,7 +888,8 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
                 cp_async4(bt + i2, p.beta + ((size_t)b * T + i) * H + h0 + hd);
             }
         }
-        for (int i2 = tp; i2 < HU * nrec; i2 += NPT) {  // decays and value scales
+        // decays and value scales (KDA: the decay vectors are read by the scan)
+        for (int i2 = tp; i2 < (C::KDA ? 0 : HU * nrec); i2 += NPT) {
             const int r = i2 % nrec, hd = i2 / nrec, hh = h0 + hd;
             if (r < hc) {
                 const size_t rec = ((size_t)b * cap + slot(r)) * H + hh;
@@ -755,7 +906,15 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
     if (named_sync_or(pc.bar_prep, NPT, false)) return false;
 
     // ---- 2. new records' decays; appends; the fp32 dot vectors
-    for (int i2 = tp; i2 < HU * T; i2 += NPT) {
+    if (C::KDA && append) {  // the drafts' decay vectors, [H][N] per record
+        constexpr int NC4 = N / 4;
+        for (int i2 = tp; i2 < T * HU * NC4; i2 += NPT) {
+            const int c = i2 % NC4, hd = (i2 / NC4) % HU, i = i2 / (NC4 * HU), hh = h0 + hd;
+            const float4 a = reinterpret_cast<const float4 *>(p.alpha + (((size_t)b * T + i) * H + hh) * N)[c];
+            reinterpret_cast<float4 *>(p.buf_a + (((size_t)b * cap + slot(hc + i)) * H + hh) * N)[c] = a;
+        }
+    }
+    for (int i2 = tp; i2 < (C::KDA ? 0 : HU * T); i2 += NPT) {
         const int i = i2 / HU, hd = i2 % HU, hh = h0 + hd, r = hc + i;
         float a;
         if (KIND == RS_MAMBA2) {  // alpha = exp(dt A), formed once when the record is appended
@@ -801,7 +960,7 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
             *reinterpret_cast<uint4 *>(qb + (jj / 8) * (KC * 128) + c * 128 + (jj % 8) * 16) = v;
         }
         fence_proxy_async_smem();  // read by the tensor cores (async proxy)
-    } else if (T > 0) {
+    } else if (T > 0 && !C::KDA) {  // (KDA: per head, after the scan)
         // one key row n per task: its JP slots as fp32, QW at a time
         for (int n = tp; n < N; n += NPT) {
 #pragma unroll
@@ -825,7 +984,7 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
     // lane = key rows lane + 32 t; the slot vectors are read once per warp
     // from the staged bf16 rows, then a recursive-halving warp reduction
     // leaves slot jj's sum in lanes jj << (5 - log2 JP)
-    if (T > 0) {
+    if (T > 0 && !C::KDA) {
         constexpr int JPP = C::JPP, NPL = N / 32, LJ = ilog2(JPP);  // padded to a power of two
         constexpr bool HOIST = NPL * JPP <= 32;
         float qv[HOIST ? NPL : 1][JPP];
@@ -879,6 +1038,9 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
     // v_s = (s < hc ? alpha_s : 1) gives E(r, hc-1) in lane r and gamma(hc-1)
     // in lane 0; each further bound m (up to hc+T-1; F-1 is among them) takes
     // one more factor: E(r, m) = E(r, m-1) alpha_m for r < m, E(m, m) = 1.
+    if constexpr (C::KDA) {
+        if (!kda_scan<C>(p, cx, L, s, b, h0, HU, pc)) return false;
+    } else
     for (int hd = pw; hd < HU; hd += C::NPW) {
         const float al = lane < nrec ? ar[hd * cap + lane] : 1.f;
         const float dtr = KIND == RS_MAMBA2 && lane < nrec ? sr[hd * cap + lane] : 1.f;
@@ -974,7 +1136,7 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
     // task per head and 4 columns, all drafts at once; the committed u come
     // from global memory, 8 records' loads in flight at a time (the first
     // task's first 8 were issued before the staging)
-    if (KIND == RS_GDN && T > 0) {
+    if (C::DELTA && T > 0) {
         for (int task = tp; task < HU * PC4; task += NPT) {
             const int hd = task / PC4, pc = task % PC4;
             float s1[TMAX][4], s2[TMAX][4];
@@ -1033,7 +1195,7 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
     constexpr int KIND = C::KIND, P = C::P, N = C::N, TMAX = C::TMAX, JP = C::JP;
     using W = WGeo<C, TE>;
     constexpr int VEC = W::VEC, RGW = W::RGW, LR = W::LR, M = W::M, NCB = W::NCB, JN = W::JN, NPASS = W::NPASS;
-    static_assert(NPASS == 1 || NPASS == 2 || (NPASS == 4 && KIND == RS_GDN), "passes");
+    static_assert(NPASS == 1 || NPASS == 2 || (NPASS == 4 && C::DELTA), "passes");
     const int lane = pc.tid & 31, warp = pc.tid >> 5;
     const int H = p.H, cap = p.cap, mode = p.mode;
     const int base = s.base, hc = s.hc, T = s.T, F = s.F;
@@ -1060,6 +1222,7 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
     const float *pre1 = reinterpret_cast<const float *>(cx + L.pre1);
     const float *pre2 = reinterpret_cast<const float *>(cx + L.pre2);
     const float *qs = reinterpret_cast<const float *>(cx + L.qs);
+    const float *gv = reinterpret_cast<const float *>(cx + L.gv), *fk = reinterpret_cast<const float *>(cx + L.fk);
 
     const int cb = warp / W::WPC;                                  // the warp's line position in a row
     const int cg = lane & (W::CPW - 1), rg = lane >> W::LCG;      // chunk among the warp's, row group
@@ -1085,6 +1248,10 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
     for (int j = 0; j < HU && ok; ++j, q0 = ring_add(q0, NCB, NS)) {
         const int hh = h0 + j;
         const size_t goff = ((size_t)b * H + hh) * ((size_t)N * P);
+        // KDA: the head's own dot vectors, per-channel products and decayed keys
+        const float *qsh = C::KDA ? qs + (size_t)j * N * JP : qs;
+        const float *gvh = C::KDA ? gv + (size_t)j * N : nullptr;
+        const float *fkh = C::KDA ? fk + (size_t)j * cap * N : nullptr;
         FoldSrc fs;
         fs.committed = static_cast<const uint8_t *>(p.buf_v) + ((size_t)b * cap * H + hh) * P * VSZ;
         fs.slot_stride = (size_t)H * P * VSZ;
@@ -1099,8 +1266,8 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
         if (T == 0) {  // flush / materialise: fold only, the head's row blocks all resident
             for (int rb = 0; rb < NCB && ok; ++rb) ok = wait_stage(full, ring_add(q0, rb, NS), abort_flag, p.status, ok);
             if (!ok) break;
-            fold_head<C, TE>(p, const_cast<uint8_t *>(stages), lane_off, q0, NS, empty, kraw, cfs, fs, fw, gF[j], F,
-                             j, row0, col0, wcol0, lcol, goff, materialize, lane, fc);
+            fold_head<C, TE>(p, const_cast<uint8_t *>(stages), lane_off, q0, NS, empty, kraw, cfs, fs, fw, gF[j], gvh,
+                             fkh, F, j, row0, col0, wcol0, lcol, goff, materialize, lane, fc);
             continue;
         }
         if (hold)
@@ -1124,12 +1291,12 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
                     }
                 }
             };
-            ok = head_pass<C, TE, 0>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qs, row0, hold);
+            ok = head_pass<C, TE, 0>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qsh, row0, hold);
             if (!ok) break;
             reduce_rows<C, TE, 1>(acc, rg);
             outputs(0);
             if constexpr (NPASS == 2) {
-                head_pass<C, TE, JN>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qs, row0, hold);
+                head_pass<C, TE, JN>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qsh, row0, hold);
                 reduce_rows<C, TE, 1>(acc, rg);
                 outputs(JN);
             }
@@ -1191,23 +1358,23 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
                 const int e = rg >> (LR - HV);
                 pp = col0 + e;
                 lead = (rg & ((1 << (LR - HV)) - 1)) == 0;
-                ok = head_pass<C, TE, 0>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qs, row0, hold);
+                ok = head_pass<C, TE, 0>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qsh, row0, hold);
                 if (!ok) break;
                 reduce_rows<C, TE, JN>(acc, rg);
 #pragma unroll
                 for (int t = 0; t < JN; ++t) sums[t] = acc[t];
                 if constexpr (NPASS >= 2) {
-                    head_pass<C, TE, JN>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qs, row0, hold);
+                    head_pass<C, TE, JN>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qsh, row0, hold);
                     reduce_rows<C, TE, JN>(acc, rg);
 #pragma unroll
                     for (int t = 0; t < JN; ++t) sums[JN + t] = acc[t];
                 }
                 if constexpr (NPASS == 4) {
-                    head_pass<C, TE, 2 * JN>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qs, row0, hold);
+                    head_pass<C, TE, 2 * JN>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qsh, row0, hold);
                     reduce_rows<C, TE, JN>(acc, rg);
 #pragma unroll
                     for (int t = 0; t < JN; ++t) sums[2 * JN + t] = acc[t];
-                    head_pass<C, TE, 3 * JN>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qs, row0, hold);
+                    head_pass<C, TE, 3 * JN>(acc, p, stages, lane_off, q0, NS, full, empty, abort_flag, qsh, row0, hold);
                     reduce_rows<C, TE, JN>(acc, rg);
 #pragma unroll
                     for (int t = 0; t < JN; ++t) sums[3 * JN + t] = acc[t];
@@ -1224,7 +1391,9 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
 #pragma unroll
                     for (int i3 = 0; i3 < TMAX; ++i3)
                         if (i3 < i) sk = fmaf(cc1[i3], ud[i3], sk);
-                    const float u = bt[i * HU + j] * (bf2f(vb[((size_t)i * HU + j) * P + pp]) - ar[j * cap + m] * sk);
+                    // (KDA: alpha_{m} is inside the dot vectors and the coefficients)
+                    const float am = C::KDA ? 1.f : ar[j * cap + m];
+                    const float u = bt[i * HU + j] * (bf2f(vb[((size_t)i * HU + j) * P + pp]) - am * sk);
                     ud[i] = u;
                     float yv = g2[j * TMAX + i] * sums[TMAX + i] + pre2[(j * TMAX + i) * P + pp];
                     const float *cc2 = c2 + (j * TMAX + i) * cap + hc;
@@ -1243,7 +1412,7 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
         if (hold) {
             if (keep)
                 fold_head<C, TE>(p, const_cast<uint8_t *>(stages), lane_off, q0, NS, empty, kraw, cfs, fs, fw, gF[j],
-                                 F, j, row0, col0, wcol0, lcol, goff, materialize, lane, fc);
+                                 gvh, fkh, F, j, row0, col0, wcol0, lcol, goff, materialize, lane, fc);
             else
                 for (int rb = 0; rb < NCB; ++rb) release_stage(empty, ring_add(q0, rb, NS));
         }
@@ -1512,12 +1681,12 @@ cudaError_t launch_pipe(const ReplayParams &p, cudaStream_t stream) {
     return launch_kernel<C, false, 1>(p, sh, dl, stream);
 }
 
-// Verify launches instantiate the draft-count buckets 1, 4 and 8 (GDN also 3).
+// Verify launches instantiate the draft-count buckets 1, 4 and 8 (GDN and KDA also 3).
 template <int KIND, int P, int N>
 cudaError_t dispatch_shape(const ReplayParams &p, cudaStream_t s) {
     const int T = p.mode == MODE_VERIFY ? p.T : 1;
     if (T <= 1) return launch_pipe<RCfg<KIND, P, N, 1>>(p, s);
-    if (KIND == RS_GDN && T <= 3) return launch_pipe<RCfg<KIND, P, N, 3>>(p, s);
+    if (KIND != RS_MAMBA2 && T <= 3) return launch_pipe<RCfg<KIND, P, N, 3>>(p, s);
     if (T <= 4) return launch_pipe<RCfg<KIND, P, N, 4>>(p, s);
     return launch_pipe<RCfg<KIND, P, N, 8>>(p, s);
 }

@@ -27,10 +27,10 @@ def to_device(d: dict, device="cuda", non_blocking: bool = False) -> dict:
 class Layer:
     def __init__(self, kind: str, B: int, H: int, G: int, P: int, N: int, L: int, T_max: int = 0,
                  capacity: int | None = None, precision: int = rb.PREC_FP32, device="cuda"):
-        if kind not in ("mamba2", "gdn"):
+        if kind not in ("mamba2", "gdn", "kda"):
             raise ValueError(f"librs has no kernels for layer kind {kind!r}")
         self.kind = kind
-        k = rb.MAMBA2 if kind == "mamba2" else rb.GDN
+        k = {"mamba2": rb.MAMBA2, "gdn": rb.GDN, "kda": rb.KDA}[kind]
         self.desc = rb.make_desc(k, B, H, G, P, N, L, T_max, capacity, precision)
         sz = rb.rs_state_bytes_for(self.desc)
         self.B, self.H, self.G, self.P, self.N, self.L, self.T_max = B, H, G, P, N, L, T_max
@@ -66,7 +66,8 @@ class Layer:
             rb.rs_decode_mamba2(self.desc, self.state, d["x"], d["dt"], params["A"], d["Bm"], d["Cm"],
                                 params.get("D"), y, stream)
         else:
-            rb.rs_decode_gdn(self.desc, self.state, d["q"], d["k"], d["v"], d["alpha"], d["beta"], y, stream)
+            fn = rb.rs_decode_gdn if self.kind == "gdn" else rb.rs_decode_kda
+            fn(self.desc, self.state, d["q"], d["k"], d["v"], d["alpha"], d["beta"], y, stream)
         return y
 
     def inputs(self, d: dict, params: dict) -> rb.Inputs:

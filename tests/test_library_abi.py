@@ -72,6 +72,8 @@ def test_state_sizes(lib):
                                     T_max=3, capacity=19, B=512))
     assert g.ckpt_hp == 512 * 32 * 128 * 128 * 4 and g.ckpt_lp == g.ckpt_hp // 2
     assert g.buf_v == 512 * 19 * 32 * 128 * 4 and g.buf_s == 0
+    k = rb.rs_state_bytes_for(_desc(kind=rb.KDA, H=32, G=16, P=128, N=128))
+    assert k.buf_a == 256 * 16 * 32 * 128 * 4 and k.buf_v == 256 * 16 * 32 * 128 * 4 and k.buf_s == 0
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -89,6 +91,10 @@ def test_state_sizes(lib):
     (dict(B=0), 1),
     (dict(B=65535, H=2048, G=8), 1),  # 2^27 slabs: beyond 32-bit-safe slab indexing
     (dict(B=65535, H=1024, G=8), 0),  # 2^26 - 2^10 slabs
+    (dict(kind=2, H=32, G=16, P=128, N=128), 0),                  # per-channel decay, fp32 checkpoint
+    (dict(kind=2, H=32, G=16, P=128, N=128, precision=1), 2),     # ... has no bf16-copy kernels
+    (dict(kind=2, H=32, G=16, P=128, N=64), 2),
+    (dict(kind=3), 1),
 ])
 def test_descriptor_validation(lib, kw, status):
     from rs_decode_gb300 import binding as rb
