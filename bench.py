@@ -124,7 +124,8 @@ def recorded_output_error() -> dict | None:
         return None
     if rec.get("source_hash") != kernel_source_hash():
         return None
-    return {k: rec[k] for k in ("two_precision", "shared_bf16", "metric", "sample", "test") if k in rec}
+    return {k: rec[k] for k in ("workload", "two_precision", "shared_bf16", "slow_decay_variant", "metric", "sample",
+                                "test") if k in rec}
 
 
 # ----------------------------------------------------------------------------- clocks

@@ -161,10 +161,14 @@ class StandardRun:
 
 
 class SpecRun:
-    """Speculative rounds (verify T drafts, then commit) on GPU and oracle."""
+    """Speculative rounds (verify T drafts, then commit) on GPU and oracle.
 
-    def __init__(self, w: synth.Workload, seed: int = 0, precision: str | None = None, sample=None):
-        self.w, self.seed = w, seed
+    ``alpha_pow`` raises every drawn decay to that power before both sides
+    see it (a slower-decaying variant of the input recipe)."""
+
+    def __init__(self, w: synth.Workload, seed: int = 0, precision: str | None = None, sample=None,
+                 alpha_pow: float | None = None):
+        self.w, self.seed, self.alpha_pow = w, seed, alpha_pow
         self.params = synth.layer_params(w, seed)
         self.gp = gpu_params(w, self.params)
         S0 = synth.initial_state(w, seed)
@@ -179,6 +183,8 @@ class SpecRun:
     def round(self, accepted: np.ndarray | None = None):
         """Returns (y_gpu, y_ref, folded[B] bool, S_before (oracle committed state))."""
         d = synth.round_inputs(self.w, self.r, self.seed, self.params)
+        if self.alpha_pow is not None:
+            d["alpha"] = np.power(d["alpha"], np.float32(self.alpha_pow)).astype(np.float32)
         if accepted is not None:
             d["accepted"] = np.asarray(accepted, np.int32)
         dev = to_device(d)

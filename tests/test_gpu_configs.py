@@ -72,11 +72,11 @@ def test_decode_full_length(name):
     assert run.layer.status() == 0
 
 
-def _spec_full(w, precision: str, idx):
+def _spec_full(w, precision: str, idx, alpha_pow=None):
     """All rounds of a speculative workload; returns per-(round, sequence)
     output errors, the fold mask and the rounds after each sequence's first
     fold."""
-    run = SpecRun(w, seed=0, precision=precision, sample=idx)
+    run = SpecRun(w, seed=0, precision=precision, sample=idx, alpha_pow=alpha_pow)
     n = len(idx)
     errs = np.zeros((w.steps, n))
     folds = np.zeros((w.steps, n), bool)
@@ -119,32 +119,51 @@ def test_mamba2_spec_full_length():
     assert folds.any(0).all(), "every sampled sequence folds at least once in 128 rounds"
 
 
-def test_gdn_spec_two_precision_full_length():
-    """Two-precision against shared-bf16 on the same inputs and sample.  Until a
-    sequence first folds, both arms read the same bf16 checkpoint values; after
-    it, the two-precision copy is a rounding of the fp32 fold while the shared
-    copy has carried bf16 rounding through every fold, so there the
-    two-precision error must not exceed the shared one."""
-    w = synth.WORKLOADS["gdn_spec"]
-    idx = parity_sample(w.B)
-    e_two, folds, after = _spec_full(w, "two", idx)
-    e_sh, folds_sh, _ = _spec_full(w, "shared_bf16", idx)
+def _precision_arms(w, idx, alpha_pow=None):
+    """Both arms on the same inputs and sample; the report of their errors."""
+    e_two, folds, after = _spec_full(w, "two", idx, alpha_pow)
+    e_sh, folds_sh, _ = _spec_full(w, "shared_bf16", idx, alpha_pow)
     assert np.array_equal(folds, folds_sh)
     assert folds.any(0).all() and after.sum() > w.steps * len(idx) // 2
     stats = lambda e, m: {"mean": float(e[m].mean()), "max": float(e[m].max()), "n": int(m.sum())}
     every = np.ones_like(after)
-    report = {
-        "workload": f"gdn_spec: B={w.B} H={w.H} G={w.G} P={w.P} N={w.N} L={w.L} T={w.T} capacity={w.cap} "
-                    f"accept={w.accept} rounds={w.steps}",
+    rep = {
+        "workload": f"{w.name}: B={w.B} H={w.H} G={w.G} P={w.P} N={w.N} L={w.L} T={w.T} capacity={w.cap} "
+                    f"accept={w.accept} rounds={w.steps}"
+                    + (f", decays alpha^{alpha_pow} of the recipe's" if alpha_pow else ""),
         "sample": f"{len(idx)} sequences incl. 0 and {w.B - 1}",
-        "metric": "per (round, sequence) normwise relative output error vs the fp64 oracle, all T drafts",
         "two_precision": {"all_rounds": stats(e_two, every), "after_first_fold": stats(e_two, after)},
         "shared_bf16": {"all_rounds": stats(e_sh, every), "after_first_fold": stats(e_sh, after)},
     }
+    return rep, e_two[after].mean(), e_sh[after].mean()
+
+
+def test_gdn_spec_two_precision_full_length():
+    """The two-precision GDN workload as specified (B = 512, 128 rounds) in
+    both arms, two-precision and shared-bf16, and the same shapes with slower
+    decays (B = 128).
+
+    Until a sequence first folds, both arms read the same bf16 checkpoint
+    values; after it, the two-precision copy is a rounding of the fp32 fold
+    while the shared copy has carried bf16 rounding through every fold.  The
+    recipe's decays (alpha = exp(-softplus(z) s), s >= 1) shrink a checkpoint
+    to about 1e-5 of itself within one 16-record window, so no rounding of it
+    survives a window and the arms agree to about 1e-4 relative: both errors
+    are reported.  With the decays raised to the power 1/50 (0.8 to 0.99 per
+    record) the checkpoint carries over windows, and there the two-precision
+    error must not exceed the shared one."""
+    w = synth.WORKLOADS["gdn_spec"]
+    rep, _, _ = _precision_arms(w, parity_sample(w.B))
+    ws = w.with_(B=128)
+    rep_slow, m_two, m_sh = _precision_arms(ws, parity_sample(ws.B), alpha_pow=0.02)
+    report = {"metric": "per (round, sequence) normwise relative output error vs the fp64 oracle, all T drafts",
+              "test": "tests/test_gpu_configs.py::test_gdn_spec_two_precision_full_length",
+              "two_precision": rep["two_precision"], "shared_bf16": rep["shared_bf16"],
+              "workload": rep["workload"], "sample": rep["sample"], "slow_decay_variant": rep_slow}
     print(json.dumps(report))
     out = os.environ.get("RS_REPORT_DIR")
     if out:
         os.makedirs(out, exist_ok=True)
         with open(os.path.join(out, "gdn_spec_output_error.json"), "w") as f:
             json.dump(report, f, indent=1)
-    assert e_two[after].mean() <= e_sh[after].mean()
+    assert m_two <= m_sh, f"slow decays: two-precision {m_two:.4e} > shared-bf16 {m_sh:.4e}"

@@ -13,8 +13,8 @@ from rs_decode_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 
-def _run_spec(w, rounds, seed=0, precision=None, sample=None, accept=None):
-    run = SpecRun(w, seed=seed, precision=precision, sample=sample)
+def _run_spec(w, rounds, seed=0, precision=None, sample=None, accept=None, alpha_pow=None):
+    run = SpecRun(w, seed=seed, precision=precision, sample=sample, alpha_pow=alpha_pow)
     prec = precision or w.precision
     errs, folds = [], []
     nfold = 0
@@ -66,10 +66,15 @@ def test_two_precision_beats_shared_bf16(kind):
     different order: tensor cores for the two-precision bf16 reads of GDN), so
     the comparison takes the rounds after each sequence's first fold, where
     the two-precision copy is a rounding of the fp32 fold and the shared one
-    has carried bf16 rounding through it."""
+    has carried bf16 rounding through it.  The GDN recipe's decays shrink a
+    checkpoint to about 1e-5 of itself within one window, so that no rounding
+    of it survives a window and the arms tie (to 1e-12 relative at B = 6);
+    its decays are slowed here to alpha^(1/50), so that the checkpoint carries
+    over windows as a slowly forgetting layer's does."""
     base = synth.WORKLOADS["gdn_spec" if kind == "gdn" else "mamba2_spec"].with_(B=6)
-    e_two, _, folds = _run_spec(base, 24, seed=3, precision="two")
-    e_shared, _, folds_sh = _run_spec(base, 24, seed=3, precision="shared_bf16")
+    ap = 0.02 if kind == "gdn" else None
+    e_two, _, folds = _run_spec(base, 24, seed=3, precision="two", alpha_pow=ap)
+    e_shared, _, folds_sh = _run_spec(base, 24, seed=3, precision="shared_bf16", alpha_pow=ap)
     assert np.array_equal(folds, folds_sh)
     first = np.where(folds.any(0), folds.argmax(0), len(folds))
     after = np.arange(len(folds))[:, None] > first[None, :]
