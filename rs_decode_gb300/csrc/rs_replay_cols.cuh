@@ -160,7 +160,7 @@ struct UnitHdr {
 // the u of the launch's own records, written and read by the same warp.
 struct RSmem {
     int stages, bars, plans, abort, tmem, d1, d2, sr, cst, fcf, unew, ctx0, ctx_bytes;
-    int hdr, kraw, ar, vb, bt, c1, c2, g1, g2, fw, gF, pre1, pre2, qs, gv, fk;  // within a context
+    int hdr, kraw, ar, vb, bt, c1, c2, g1, g2, fw, gF, pre1, qs, gv, fk;  // within a context
     int total;
 };
 
@@ -204,8 +204,8 @@ __host__ __device__ inline RSmem replay_smem(int cap, int HU, int NS) {
     s.g2 = c;     c += al16(HU * TMAX * 4);
     s.fw = c;     c += al16(HU * cap * 4);
     s.gF = c;     c += al16(HU * 4);
-    s.pre1 = c;   c += al16(HU * TMAX * P * 4);                     // record parts of the outputs
-    s.pre2 = c;   c += GDN ? al16(HU * TMAX * P * 4) : 0;
+    // Mamba-2: record parts of the outputs (GDN, KDA: summed by the consumer warps)
+    s.pre1 = c;   c += GDN ? 0 : al16(HU * TMAX * P * 4);
     // fp32 dot vectors [QC][N][QW] (KDA: one set per head), or (tensor-core
     // units) the bf16 B operand
     s.qs = c;     c += al16(KDA ? HU * N * C::JP * 4 : (C::UMMA && C::QB_BYTES > N * C::JP * 4 ? C::QB_BYTES : N * C::JP * 4));
@@ -724,13 +724,42 @@ __device__ __forceinline__ bool kda_scan(const ReplayParams &p, uint8_t *cx, con
 #pragma unroll
             for (int i = 0; i < TMAX; ++i) Pd[i][t] = 1.f;
         }
-        for (int r = nrec - 1; r >= 0; --r) {
-            const float *asrc = r < hc ? p.buf_a + (((size_t)b * cap + slot(r)) * H + hh) * N
-                                       : p.alpha + (((size_t)b * T + (r - hc)) * H + hh) * N;
+        // the drafts' keys and queries at the lane's channels, read once (up to
+        // four drafts; more are read per record)
+        constexpr bool HOIST = TMAX <= 4;
+        float kd[HOIST ? TMAX : 1][NPL], qd[HOIST ? TMAX : 1][NPL];
+        if constexpr (HOIST) {
+#pragma unroll
+            for (int i = 0; i < TMAX; ++i)
+#pragma unroll
+                for (int t = 0; t < NPL; ++t) {
+                    kd[i][t] = i < T ? bf2f(kraw[(size_t)(hc + i) * N + lane + 32 * t]) : 0.f;
+                    qd[i][t] = i < T ? bf2f(kraw[(size_t)(cap + i) * N + lane + 32 * t]) : 0.f;
+                }
+        }
+        // the records' decay vectors are loaded CA records at a time, ahead of
+        // their use (they come from L2 or HBM; the scan is sequential)
+        constexpr int CA = TMAX <= 4 ? 8 : 4;
+        for (int rc = nrec - 1; rc >= 0; rc -= CA) {
+            float ac[CA][NPL];
+#pragma unroll
+            for (int q = 0; q < CA; ++q) {
+                const int r = rc - q;
+                if (r >= 0) {
+                    const float *asrc = r < hc ? p.buf_a + (((size_t)b * cap + slot(r)) * H + hh) * N
+                                               : p.alpha + (((size_t)b * T + (r - hc)) * H + hh) * N;
+#pragma unroll
+                    for (int t = 0; t < NPL; ++t) ac[q][t] = asrc[lane + 32 * t];
+                }
+            }
+#pragma unroll
+        for (int q = 0; q < CA; ++q) {
+            const int r = rc - q;
+            if (r < 0) break;
             float a[NPL], kr[NPL];
 #pragma unroll
             for (int t = 0; t < NPL; ++t) {
-                a[t] = asrc[lane + 32 * t];
+                a[t] = ac[q][t];
                 kr[t] = bf2f(kraw[(size_t)r * N + lane + 32 * t]);
             }
             if (T > 0) {
@@ -745,8 +774,10 @@ __device__ __forceinline__ bool kda_scan(const ReplayParams &p, uint8_t *cx, con
                         for (int t = 0; t < NPL; ++t) {
                             const int n = lane + 32 * t;
                             const float wk = Pd[i][t] * kr[t];
-                            v[i] = fmaf(wk, bf2f(kraw[(size_t)(hc + i) * N + n]), v[i]);
-                            v[TMAX + i] = fmaf(wk, bf2f(kraw[(size_t)(cap + i) * N + n]), v[TMAX + i]);
+                            const float kv = HOIST ? kd[HOIST ? i : 0][t] : bf2f(kraw[(size_t)(hc + i) * N + n]);
+                            const float qv = HOIST ? qd[HOIST ? i : 0][t] : bf2f(kraw[(size_t)(cap + i) * N + n]);
+                            v[i] = fmaf(wk, kv, v[i]);
+                            v[TMAX + i] = fmaf(wk, qv, v[TMAX + i]);
                         }
                     }
                 }
@@ -773,6 +804,7 @@ __device__ __forceinline__ bool kda_scan(const ReplayParams &p, uint8_t *cx, con
                     if (i < T && r <= hc + i) Pd[i][t] *= a[t];
                 if (r < F) PF[t] *= a[t];
             }
+        }
         }
         // the running products are now gamma(m_i) and gamma(F - 1)
         float *qh = qs + (size_t)hd * N * JP;
@@ -826,7 +858,7 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
     float *c1 = reinterpret_cast<float *>(cx + L.c1), *c2 = reinterpret_cast<float *>(cx + L.c2);
     float *g1 = reinterpret_cast<float *>(cx + L.g1), *g2 = reinterpret_cast<float *>(cx + L.g2);
     float *fw = reinterpret_cast<float *>(cx + L.fw), *gF = reinterpret_cast<float *>(cx + L.gF);
-    float *pre1 = reinterpret_cast<float *>(cx + L.pre1), *pre2 = reinterpret_cast<float *>(cx + L.pre2);
+    float *pre1 = reinterpret_cast<float *>(cx + L.pre1);
     float *qs = reinterpret_cast<float *>(cx + L.qs);
 
     // Mamba-2 step-5 task of this thread (one head, 8 value columns): the first
@@ -842,18 +874,6 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
     uint4 xv[8];
 #pragma unroll
     for (int t = 0; t < 8; ++t) xv[t] = x_task && t < nrec ? ld_u4(x_src(t)) : make_uint4(0u, 0u, 0u, 0u);
-    // GDN step-5 tasks (one head, 4 value columns): the committed u of the
-    // first 8 records, likewise loaded before the staging
-    constexpr int PC4 = P / 4;
-    const float *ubuf = static_cast<const float *>(p.buf_v);
-    auto u_src = [&](int task, int r) {
-        return ubuf + (((size_t)b * cap + slot(r)) * H + h0 + task / PC4) * P + 4 * (task % PC4);
-    };
-    const bool u_pre = C::DELTA && T > 0 && tp < HU * PC4;
-    float4 uv[8];
-#pragma unroll
-    for (int t = 0; t < 8; ++t)
-        uv[t] = u_pre && t < hc ? *reinterpret_cast<const float4 *>(u_src(tp, t)) : make_float4(0.f, 0.f, 0.f, 0.f);
 
     // ---- 1. one batch of cp.async copies for every small operand of the unit
     {
@@ -1132,55 +1152,8 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
         }
         if (named_sync_or(pc.bar_prep, NPT, false)) return false;
     }
-    // GDN: committed-record parts of S_{m_i-1} k_{m_i} and S_{m_i} q_i: one
-    // task per head and 4 columns, all drafts at once; the committed u come
-    // from global memory, 8 records' loads in flight at a time (the first
-    // task's first 8 were issued before the staging)
-    if (C::DELTA && T > 0) {
-        for (int task = tp; task < HU * PC4; task += NPT) {
-            const int hd = task / PC4, pc = task % PC4;
-            float s1[TMAX][4], s2[TMAX][4];
-#pragma unroll
-            for (int i = 0; i < TMAX; ++i)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) s1[i][e] = s2[i][e] = 0.f;
-            for (int r0 = 0; r0 < hc; r0 += 8) {
-                if (r0 > 0 || task != tp) {
-#pragma unroll
-                    for (int t = 0; t < 8; ++t)
-                        uv[t] = r0 + t < hc ? *reinterpret_cast<const float4 *>(u_src(task, r0 + t))
-                                            : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    const int r = r0 + t;
-                    if (r >= hc) break;
-                    const float u[4] = {uv[t].x, uv[t].y, uv[t].z, uv[t].w};
-#pragma unroll
-                    for (int i = 0; i < TMAX; ++i) {
-                        if (i < T) {
-                            const float a1 = c1[(hd * TMAX + i) * cap + r], a2 = c2[(hd * TMAX + i) * cap + r];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                s1[i][e] = fmaf(a1, u[e], s1[i][e]);
-                                s2[i][e] = fmaf(a2, u[e], s2[i][e]);
-                            }
-                        }
-                    }
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < TMAX; ++i) {
-                if (i < T) {
-                    *reinterpret_cast<float4 *>(pre1 + (hd * TMAX + i) * P + 4 * pc) =
-                        make_float4(s1[i][0], s1[i][1], s1[i][2], s1[i][3]);
-                    *reinterpret_cast<float4 *>(pre2 + (hd * TMAX + i) * P + 4 * pc) =
-                        make_float4(s2[i][0], s2[i][1], s2[i][2], s2[i][3]);
-                }
-            }
-        }
-        if (named_sync_or(pc.bar_prep, NPT, false)) return false;
-    }
+    // (GDN, KDA: the committed-record parts of S_{m_i-1} k_{m_i} and S_{m_i} q_i
+    // are summed by the consumer warps, each for its own columns)
     return true;
 }
 
@@ -1220,7 +1193,6 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
     const float *g1 = reinterpret_cast<const float *>(cx + L.g1), *g2 = reinterpret_cast<const float *>(cx + L.g2);
     const float *fw = reinterpret_cast<const float *>(cx + L.fw), *gF = reinterpret_cast<const float *>(cx + L.gF);
     const float *pre1 = reinterpret_cast<const float *>(cx + L.pre1);
-    const float *pre2 = reinterpret_cast<const float *>(cx + L.pre2);
     const float *qs = reinterpret_cast<const float *>(cx + L.qs);
     const float *gv = reinterpret_cast<const float *>(cx + L.gv), *fk = reinterpret_cast<const float *>(cx + L.fk);
 
@@ -1307,6 +1279,18 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
             float sums[JP];
             int pp;
             bool lead;
+            // The committed records' parts, per draft i: rs1[i] = sum_{r<hc}
+            // c1[i][r] u_r[pp] (of S_{m_i-1} k_{m_i}) and rs2[i] = sum c2[i][r] u_r[pp]
+            // (of S_{m_i} q_i), for the column the lane holds after the dots; the
+            // first UPF records' u are loaded now, so that their latency overlaps
+            // the dots (the tensor cores' or the lane's own).
+            constexpr int UPF = 8;
+            const int pl = (TC && C::UMMA && sizeof(TE) == 2) ? 32 * warp + lane : col0 + (rg >> (LR - ilog2(VEC)));
+            const float *ucol = static_cast<const float *>(p.buf_v) + ((size_t)b * cap * H + hh) * P + pl;
+            const size_t ustride = (size_t)H * P;
+            float upf[UPF];
+#pragma unroll
+            for (int t = 0; t < UPF; ++t) upf[t] = t < hc ? ucol[slot(t) * ustride] : 0.f;
             if constexpr (TC && C::UMMA && sizeof(TE) == 2) {
                 // Tensor cores: D[p][jj] = sum_n S_c[n][p] v_jj[n] for the head's
                 // two row blocks (M = 128 value columns, K = N keys, A read from
@@ -1380,13 +1364,35 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
                     for (int t = 0; t < JN; ++t) sums[3 * JN + t] = acc[t];
                 }
             }
+            float rs1[TMAX], rs2[TMAX];
+#pragma unroll
+            for (int i = 0; i < TMAX; ++i) rs1[i] = rs2[i] = 0.f;
+            for (int r0 = 0; r0 < hc; r0 += UPF) {
+                if (r0 > 0) {
+#pragma unroll
+                    for (int t = 0; t < UPF; ++t) upf[t] = r0 + t < hc ? ucol[slot(r0 + t) * ustride] : 0.f;
+                }
+#pragma unroll
+                for (int t = 0; t < UPF; ++t) {
+                    const int r = r0 + t;
+                    if (r < hc) {
+#pragma unroll
+                        for (int i = 0; i < TMAX; ++i) {
+                            if (i < T) {
+                                rs1[i] = fmaf(c1[(j * TMAX + i) * cap + r], upf[t], rs1[i]);
+                                rs2[i] = fmaf(c2[(j * TMAX + i) * cap + r], upf[t], rs2[i]);
+                            }
+                        }
+                    }
+                }
+            }
             float ud[TMAX];
 #pragma unroll
             for (int i = 0; i < TMAX; ++i) {
                 ud[i] = 0.f;
                 if (i < T) {
                     const int m = hc + i;
-                    float sk = g1[j * TMAX + i] * sums[i] + pre1[(j * TMAX + i) * P + pp];
+                    float sk = g1[j * TMAX + i] * sums[i] + rs1[i];
                     const float *cc1 = c1 + (j * TMAX + i) * cap + hc;
 #pragma unroll
                     for (int i3 = 0; i3 < TMAX; ++i3)
@@ -1395,7 +1401,7 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
                     const float am = C::KDA ? 1.f : ar[j * cap + m];
                     const float u = bt[i * HU + j] * (bf2f(vb[((size_t)i * HU + j) * P + pp]) - am * sk);
                     ud[i] = u;
-                    float yv = g2[j * TMAX + i] * sums[TMAX + i] + pre2[(j * TMAX + i) * P + pp];
+                    float yv = g2[j * TMAX + i] * sums[TMAX + i] + rs2[i];
                     const float *cc2 = c2 + (j * TMAX + i) * cap + hc;
 #pragma unroll
                     for (int i3 = 0; i3 < TMAX; ++i3)
