@@ -87,10 +87,18 @@ def _code_only(text: str) -> str:
     return "\n".join(ln for ln in lines if ln.strip())
 
 
-def kernel_source_hash() -> str:
+# The sources each workload's replay kernel is built from (the launch entry,
+# the planning and device helpers, the pipeline, the family's translation unit).
+KERNEL_SOURCES = {
+    "mamba2": ("rs_internal.h", "rs_common.cuh", "rs_plan.cuh", "rs_replay_rows.cuh", "rs_replay.cu", "rs_replay_m2.cu"),
+    "gdn": ("rs_internal.h", "rs_common.cuh", "rs_plan.cuh", "rs_replay_cols.cuh", "rs_replay.cu", "rs_replay_gdn.cu"),
+    "kda": ("rs_internal.h", "rs_common.cuh", "rs_plan.cuh", "rs_replay_cols.cuh", "rs_replay.cu", "rs_replay_kda.cu"),
+}
+
+
+def kernel_source_hash(workload: str) -> str:
     h = hashlib.sha256()
-    for name in ("rs_plan.cuh", "rs_replay_rows.cuh", "rs_replay_cols.cuh", "rs_replay.cu", "rs_replay_m2.cu",
-                 "rs_replay_gdn.cu", "rs_replay_kda.cu", "rs_common.cuh"):
+    for name in KERNEL_SOURCES[workload]:
         with open(os.path.join(ROOT, "rs_decode_gb300", "csrc", name), encoding="utf-8") as f:
             h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
@@ -105,7 +113,7 @@ def profiled_traffic(workload: str) -> float | None:
             rec = json.load(f)
     except OSError:
         return None
-    if rec.get("source_hash") != kernel_source_hash():
+    if rec.get("source_hash") != kernel_source_hash(workload):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -122,7 +130,7 @@ def recorded_output_error() -> dict | None:
             rec = json.load(f)
     except OSError:
         return None
-    if rec.get("source_hash") != kernel_source_hash():
+    if rec.get("source_hash") != kernel_source_hash("gdn"):
         return None
     return {k: rec[k] for k in ("workload", "two_precision", "shared_bf16", "slow_decay_variant", "metric", "sample",
                                 "test") if k in rec}

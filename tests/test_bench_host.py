@@ -136,3 +136,15 @@ def test_algorithmic_bytes_with_per_channel_decay():
     rec, inp, out, ck = 16 * 1024 + 16 * 1024 + 4096, 16 * 1024 + 16 * 1024 + 128, 16 * 1024, 2 * 2**20
     assert avg(k) == 256 * (ck + ck / 16 + 7.5 * rec + 15 / 16 * rec + inp + out)
     assert 1.05 < avg(k) / avg(g) < 1.08
+
+
+def test_traffic_records_are_keyed_by_their_kernels_sources():
+    """A workload's recorded DRAM traffic stays valid while the sources its
+    replay kernel is built from are unchanged: the row-split pipeline for
+    Mamba-2, the column-split one for GDN and the per-channel decay."""
+    assert "rs_replay_rows.cuh" in bench.KERNEL_SOURCES["mamba2"]
+    assert "rs_replay_cols.cuh" not in bench.KERNEL_SOURCES["mamba2"]
+    for wl in ("gdn", "kda"):
+        assert "rs_replay_cols.cuh" in bench.KERNEL_SOURCES[wl]
+        assert "rs_replay_rows.cuh" not in bench.KERNEL_SOURCES[wl]
+    assert len({bench.kernel_source_hash(w) for w in ("mamba2", "gdn", "kda")}) == 3
