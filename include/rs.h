@@ -133,7 +133,8 @@ typedef struct {
     int32_t *base;     /* [B] slot of the first record after the checkpoint          */
     int32_t *h;        /* [B] committed records after the checkpoint                 */
     int32_t *nd;       /* [B] appended, not yet accepted draft records               */
-    uint32_t *arrive;  /* [B] per-sequence arrival counters (kernel scratch)         */
+    uint32_t *arrive;  /* [B + 2] per-sequence arrival counters and the launch's two
+                          unit-scheduling counters (kernel scratch; rs_init clears it) */
     uint32_t *status;  /* [1] device status word (RS_DEV_* bits)                     */
 } rs_state;
 
@@ -321,7 +322,8 @@ rs_status rs_eager_select(const rs_layer_desc *desc, int32_t *cur, const int32_t
  * that only receives pre-planned tensors, or a server that forbids device
  * allocation after start-up.  The per-sequence arrival counters, which
  * rs_decode_mamba2 keeps in st->arrive (that member is ignored here and may be
- * NULL), live in a 16 KiB static device array of this library instead.
+ * NULL), live in a static device array of this library instead (4096 counters
+ * and the two unit-scheduling counters: 16 KiB + 8 bytes).
  *   - B <= RS_STATIC_MAX_SEQS, else RS_ERR_STATIC_LIMIT and nothing is enqueued.
  *   - The first call in a device context looks up the array's address with
  *     that device current; make it before any stream capture.  The address is

@@ -143,7 +143,8 @@ rs_status rs_state_bytes_for(const rs_layer_desc *d, rs_state_bytes *o) {
     o->buf_k = B * C * G * N * 2;
     o->buf_a = B * C * H * (d->kind == RS_KDA ? N : 1) * 4;
     o->buf_s = d->kind == RS_MAMBA2 ? B * C * H * 4 : 0;
-    o->base = o->h = o->nd = o->arrive = B * 4;
+    o->base = o->h = o->nd = B * 4;
+    o->arrive = (B + 2) * 4;  // per-sequence arrival counters + the launch's two scheduling counters
     o->status = 4;
     return RS_OK;
 }

@@ -46,6 +46,11 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
 }
 
+// Brings the 128-byte line holding p into L2 (no register, no wait).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // An always-zero value that the compiler cannot see through; adding it to an
 // address makes a later memory operation wait for the loads that produced x.
 __device__ __forceinline__ unsigned zero_dependent_on(unsigned x) {

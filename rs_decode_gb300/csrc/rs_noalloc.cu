@@ -4,8 +4,9 @@
 //
 // The replay kernel needs one piece of scratch: a per-sequence arrival counter
 // (rs_state.arrive) that tells the last work unit of a sequence to advance
-// its pointers.  Some callers have no way to provide it: an inference-engine
-// plugin whose host framework only passes the tensors it planned up front,
+// its pointers, followed by the launch's two unit-scheduling counters.  Some
+// callers have no way to provide it: an inference-engine plugin whose host
+// framework only passes the tensors it planned up front,
 // or a runtime that forbids device allocation once serving starts because
 // its memory plan is fixed.  This entry point keeps those counters in a
 // file-scope device array instead, so it needs (and allocates) nothing.
@@ -14,7 +15,7 @@
 //  * at most kStaticMaxSeqs (4096) sequences per call; larger B returns
 //    RS_ERR_STATIC_LIMIT before anything is enqueued;
 //  * the array exists once per device that loads the library and lives until
-//    the process exits (16 KiB);
+//    the process exits (16 KiB + 8 bytes);
 //  * the first call in a device context looks up the array's device address
 //    (cudaGetSymbolAddress) with that device current; make that first call
 //    before any stream capture.  The address is cached per device and tagged
@@ -39,7 +40,8 @@ namespace {
 constexpr int kStaticMaxSeqs = RS_STATIC_MAX_SEQS;
 
 // Zero-initialised when the module loads on a device; cleared again per call.
-static __device__ __align__(256) uint32_t g_arrive[kStaticMaxSeqs];
+// kStaticMaxSeqs arrival counters and the two scheduling counters.
+static __device__ __align__(256) uint32_t g_arrive[kStaticMaxSeqs + 2];
 
 // The current context's unique ID (cuCtxGetCurrent + cuCtxGetId, fetched from
 // the driver through the runtime: no link-time dependency on the driver
@@ -115,7 +117,8 @@ extern "C" rs_status rs_decode_mamba2_noalloc(const rs_layer_desc *d, const rs_s
     uint32_t *arrive = nullptr;
     if ((s = static_arrive(&arrive)) != RS_OK) return s;
     cudaStream_t cs = (cudaStream_t)stream;
-    if ((s = rs::cuda_status(cudaMemsetAsync(arrive, 0, sizeof(uint32_t) * (size_t)d->B, cs))) != RS_OK) return s;
+    if ((s = rs::cuda_status(cudaMemsetAsync(arrive, 0, sizeof(uint32_t) * ((size_t)d->B + 2), cs))) != RS_OK)
+        return s;
 
     rs::ReplayParams p = {};
     p.B = d->B; p.H = d->H; p.G = d->G; p.L = d->L; p.cap = d->capacity; p.T = 1;

@@ -85,6 +85,24 @@ __device__ __forceinline__ void arrive_and_update(const ReplayParams &p, const S
     }
 }
 
+// Dynamic unit scheduling.  A launch's units are handed out in order from one
+// counter, arrive[B]: each pipeline takes its next unit when its planner is
+// ready for one, so that a pipeline that drew costly units (a folding unit
+// moves several times the bytes of a streamed one, and which sequences fold
+// depends on their pointers) takes fewer.  The planners finish by counting
+// themselves on arrive[B + 1]; the last one resets both counters for the next
+// launch on the state.
+__device__ __forceinline__ int next_unit(const ReplayParams &p) {
+    return (int)atomicAdd(p.arrive + p.B, 1u);
+}
+__device__ __forceinline__ void planner_done(const ReplayParams &p, unsigned planners) {
+    uint32_t *ctr = p.arrive + p.B;
+    if (atomicAdd(ctr + 1, 1u) == planners - 1) {
+        ctr[0] = 0u;
+        ctr[1] = 0u;
+    }
+}
+
 // Two-precision: a folding sequence reads the fp32 copy, any other the bf16
 // copy; shared-bf16 has only the bf16 copy.
 __device__ __forceinline__ bool plan_reads_lp(const ReplayParams &p, const SeqPlan &s) {

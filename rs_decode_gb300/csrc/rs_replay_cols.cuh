@@ -238,7 +238,8 @@ __host__ __device__ inline int pipe_bytes(const RSmem &L) { return (L.total + 10
 // two side by side (2 NT threads, two carve-ups): kernels that hold tensor
 // memory are resident one CTA per SM, so they pair their pipelines in one CTA.
 struct PipeCtx {
-    int u0, ustride;        // the pipeline's units: u0, u0 + ustride, ...
+    int u0;                 // the pipeline's index in the grid
+    int planners;           // pipelines in the grid (each plans its own units)
     int tid;                // thread index within the pipeline
     int bar_prep;           // named barrier of the pipeline's prep warps
     bool tc;                // bf16 blocks are dotted on the tensor cores
@@ -346,11 +347,12 @@ __device__ __forceinline__ void reduce_rows(float (&acc)[WGeo<C, TE>::M], int rg
 }
 
 // ---------------------------------------------------------------------------
-// Planner (one lane of the producer warp): reads each unit's pointers, takes
-// part in the pointer update, and hands the plan to the prep warps through a
-// ring of kPlanRing slots, so that the pointer reads and the arrival atomic of
-// later units overlap the prep warps' work on the current one.  A plan with
-// b = -1 ends the pipeline.
+// Planner (one lane of the producer warp): takes the pipeline's next unit from
+// the launch's counter (dynamic scheduling, rs_plan.cuh), reads its pointers,
+// takes part in the pointer update, and hands the plan to the prep warps
+// through a ring of kPlanRing slots, so that the pointer reads and the arrival
+// atomic of later units overlap the prep warps' work on the current one.  A
+// plan with b = -1 ends the pipeline.
 template <class C>
 __device__ __forceinline__ void planner(const ReplayParams &p, uint8_t *sm, const RSmem &L, int units, int HU,
                                         int NS, const PipeCtx &pc) {
@@ -358,12 +360,17 @@ __device__ __forceinline__ void planner(const ReplayParams &p, uint8_t *sm, cons
     UnitHdr *plans = reinterpret_cast<UnitHdr *>(sm + L.plans);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
     const unsigned upseq = p.H / HU;
-    for (int cu = 0, u = pc.u0;; ++cu, u += pc.ustride) {
+    for (int cu = 0;; ++cu) {
         const int slot = cu % kPlanRing;
-        if (!wait_or_abort(pempty + slot, ((cu / kPlanRing) & 1) ^ 1, abort_flag, p.status)) return;
+        if (!wait_or_abort(pempty + slot, ((cu / kPlanRing) & 1) ^ 1, abort_flag, p.status)) {
+            planner_done(p, pc.planners);
+            return;
+        }
+        const int u = next_unit(p);
         if (u >= units) {
             plans[slot].b = -1;
             mbar_arrive(pfull + slot);
+            planner_done(p, pc.planners);
             return;
         }
         const int b = u / upseq;
@@ -875,6 +882,18 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
 #pragma unroll
     for (int t = 0; t < 8; ++t) xv[t] = x_task && t < nrec ? ld_u4(x_src(t)) : make_uint4(0u, 0u, 0u, 0u);
 
+    // KDA: the records' decay vectors (N fp32 per head and record) are read by
+    // the sequential scan; bring their lines into L2 now, so that they arrive
+    // while the staging below waits
+    if (C::KDA) {
+        constexpr int LPV = N * 4 / 128;  // 128-byte lines per decay vector
+        for (int i2 = tp; i2 < HU * nrec * LPV; i2 += NPT) {
+            const int l = i2 % LPV, r = (i2 / LPV) % nrec, hh = h0 + i2 / (LPV * nrec);
+            const float *src = r < hc ? p.buf_a + (((size_t)b * cap + slot(r)) * H + hh) * N
+                                      : p.alpha + (((size_t)b * T + (r - hc)) * H + hh) * N;
+            prefetch_l2(src + l * 32);
+        }
+    }
     // ---- 1. one batch of cp.async copies for every small operand of the unit
     {
         constexpr int KC = N / 8;  // 16-byte chunks per key row
@@ -1510,7 +1529,7 @@ __global__ void __launch_bounds__(C::NT * PIPES, PIPES == 1 ? C::MIN_BLOCKS : 1)
     uint8_t *sm = sm0 + (size_t)pipe * pipe_bytes(L);
     PipeCtx pc;
     pc.u0 = blockIdx.x * PIPES + pipe;
-    pc.ustride = gridDim.x * PIPES;
+    pc.planners = gridDim.x * PIPES;
     pc.tid = threadIdx.x & (C::NT - 1);
     pc.bar_prep = 1 + pipe;  // named barriers 1 .. PIPES; PIPES + 1: every consumer warp of the CTA
     pc.tc = TC;

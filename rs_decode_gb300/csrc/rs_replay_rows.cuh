@@ -27,6 +27,9 @@
 // owns VEC value columns of R consecutive key rows, so its dot products
 // accumulate locally and only a per-head cross-warp reduction is needed.
 //
+// Units are handed out dynamically (the launch's unit counter, rs_plan.cuh):
+// the producer takes its CTA's next unit when it plans one and passes the
+// unit's place to the consumers with the plan; an end plan (b = -1) ends them.
 // Per-sequence pointers (base, h, nd) are read once per unit by the producer;
 // the last unit to have read them (an arrival counter) writes the new values,
 // so no second launch is needed.  Every wait is bounded: on a time-out the CTA
@@ -52,6 +55,12 @@ struct PipeCfg {
     static constexpr int MIN_BLOCKS = (NS <= 2 && TMAX <= 4) ? 2 : 1;
 };
 
+// A unit's plan as the producer hands it to the consumers (b = -1: no more units).
+struct RowPlan {
+    SeqPlan s;
+    int b, h0;
+};
+
 // Shared-memory carve-up, byte offsets (16-byte aligned; stages first).
 struct PipeSmem {
     int stages, bars, plans, abort, kraw, xr, ar, sr, cst, vb, bt, d1, d2, c1, c2, g1, g2, fw, gF, pre1, pre2, red,
@@ -68,7 +77,7 @@ __host__ __device__ inline PipeSmem pipe_smem(int cap) {
     int o = 0;
     s.stages = o; o += C::NS * C::STAGE;
     s.bars = o;   o += al16((2 * C::NS + 4) * 8);
-    s.plans = o;  o += al16(2 * (int)sizeof(SeqPlan));
+    s.plans = o;  o += al16(2 * (int)sizeof(RowPlan));
     s.abort = o;  o += 16;
     s.kraw = o;   o += al16((cap + TMAX) * N * 2);                  // bf16 keys (rows < cap), queries (cap + i)
     s.xr = o;     o += al16(HU * cap * P * (GDN ? 4 : 2));          // Mamba-2 x bf16 / GDN u fp32 per record
@@ -114,28 +123,32 @@ __device__ __forceinline__ void load_bf16_run(const uint16_t *src, float (&out)[
 }
 
 // ---------------------------------------------------------------------------
-// Producer: plan each unit, publish the plan, stream the unit's row blocks.
+// Producer: take each unit from the launch's counter, plan it, publish the
+// plan, stream the unit's row blocks; then publish the end plan.
 template <class C>
 __device__ __forceinline__ void producer(const ReplayParams &p, uint8_t *sm, const PipeSmem &L, int units) {
     constexpr int HU = C::HU, NS = C::NS, N = C::N, P = C::P, SPLIT = C::SPLIT;
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + L.bars), *empty = full + NS;
     uint64_t *pfull = empty + NS, *pempty = pfull + 2;
-    SeqPlan *plans = reinterpret_cast<SeqPlan *>(sm + L.plans);
+    RowPlan *plans = reinterpret_cast<RowPlan *>(sm + L.plans);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
     const unsigned upseq = p.H / HU;
     int it = 0, pu = 0;
-    int u = blockIdx.x;
+    int u = next_unit(p);
     SeqPlan cur;
     if (u < units) {
         cur = plan_sequence(p, u / upseq);
         arrive_and_update(p, cur, u / upseq, upseq, (u % upseq) == 0);
     }
-    for (; u < units; u += gridDim.x, ++pu) {
+    bool stop = false;
+    for (; u < units; ++pu) {
         const int b = u / upseq, h0 = (u % upseq) * HU;
-        if (!wait_or_abort(pempty + (pu & 1), ((pu >> 1) & 1) ^ 1, abort_flag, p.status)) break;
-        plans[pu & 1] = cur;
+        if (!wait_or_abort(pempty + (pu & 1), ((pu >> 1) & 1) ^ 1, abort_flag, p.status)) { stop = true; break; }
+        plans[pu & 1].s = cur;
+        plans[pu & 1].b = b;
+        plans[pu & 1].h0 = h0;
         mbar_arrive(pfull + (pu & 1));  // release: the plan is visible to the consumers
-        const int un = u + gridDim.x;
+        int un = units;
         SeqPlan next;
         bool planned = false;
         if (cur.work) {
@@ -144,26 +157,37 @@ __device__ __forceinline__ void producer(const ReplayParams &p, uint8_t *sm, con
             const uint8_t *src = (lp ? reinterpret_cast<const uint8_t *>(p.ckpt_lp)
                                      : reinterpret_cast<const uint8_t *>(p.ckpt_hp)) +
                                  ((size_t)b * p.H + h0) * slab;
-            bool stop = false;
             for (int q = 0; q < HU * SPLIT; ++q, ++it) {
                 const int st = it % NS;
                 if (!wait_or_abort(empty + st, ((it / NS) & 1) ^ 1, abort_flag, p.status)) { stop = true; break; }
                 mbar_arrive_expect_tx(full + st, part);
                 bulk_copy_g2s(sm + L.stages + (size_t)st * C::STAGE, src + (size_t)q * part, part, full + st);
-                if (q == 0 && un < units) {  // plan the next unit while this one streams
-                    next = plan_sequence(p, un / upseq);
-                    arrive_and_update(p, next, un / upseq, upseq, (un % upseq) == 0);
+                if (q == 0) {  // plan the next unit while this one streams
+                    un = next_unit(p);
+                    if (un < units) {
+                        next = plan_sequence(p, un / upseq);
+                        arrive_and_update(p, next, un / upseq, upseq, (un % upseq) == 0);
+                    }
                     planned = true;
                 }
             }
             if (stop) break;
         }
-        if (un < units && !planned) {
-            next = plan_sequence(p, un / upseq);
-            arrive_and_update(p, next, un / upseq, upseq, (un % upseq) == 0);
+        if (!planned) {
+            un = next_unit(p);
+            if (un < units) {
+                next = plan_sequence(p, un / upseq);
+                arrive_and_update(p, next, un / upseq, upseq, (un % upseq) == 0);
+            }
         }
+        u = un;
         cur = next;
     }
+    if (!stop && wait_or_abort(pempty + (pu & 1), ((pu >> 1) & 1) ^ 1, abort_flag, p.status)) {
+        plans[pu & 1].b = -1;  // the end plan
+        mbar_arrive(pfull + (pu & 1));
+    }
+    planner_done(p, gridDim.x);
     if (*abort_flag) {
         // drain: wait (bounded) for the copies this thread may still have in flight
         for (int k = it - NS > 0 ? it - NS : 0; k < it; ++k) mbar_wait(full + k % NS, (k / NS) & 1);
@@ -661,22 +685,21 @@ __device__ __forceinline__ bool consume_unit(const ReplayParams &p, uint8_t *sm,
 }
 
 template <class C>
-__device__ __forceinline__ void consumer(const ReplayParams &p, uint8_t *sm, const PipeSmem &L, int units) {
+__device__ __forceinline__ void consumer(const ReplayParams &p, uint8_t *sm, const PipeSmem &L) {
     uint64_t *pfull = reinterpret_cast<uint64_t *>(sm + L.bars) + 2 * C::NS, *pempty = pfull + 2;
-    SeqPlan *plans = reinterpret_cast<SeqPlan *>(sm + L.plans);
+    const RowPlan *plans = reinterpret_cast<const RowPlan *>(sm + L.plans);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
-    const unsigned upseq = p.H / C::HU;
-    int it = 0, pu = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++pu) {
+    int it = 0;
+    for (int pu = 0;; ++pu) {
         const bool ok = wait_or_abort(pfull + (pu & 1), (pu >> 1) & 1, abort_flag, p.status);
-        SeqPlan s;
-        if (ok) s = plans[pu & 1];
+        RowPlan rp;
+        if (ok) rp = plans[pu & 1];
         if (named_sync_or(1, C::NC, !ok)) return;
         if (threadIdx.x == 0) mbar_arrive(pempty + (pu & 1));
-        if (!s.work) continue;
-        const int b = u / upseq, h0 = (u % upseq) * C::HU;
-        const bool done = plan_reads_lp(p, s) ? consume_unit<C, uint16_t>(p, sm, L, s, b, h0, it)
-                                              : consume_unit<C, float>(p, sm, L, s, b, h0, it);
+        if (rp.b < 0) return;  // the end plan
+        if (!rp.s.work) continue;
+        const bool done = plan_reads_lp(p, rp.s) ? consume_unit<C, uint16_t>(p, sm, L, rp.s, rp.b, rp.h0, it)
+                                                 : consume_unit<C, float>(p, sm, L, rp.s, rp.b, rp.h0, it);
         if (!done) return;
     }
 }
@@ -703,7 +726,7 @@ __global__ void __launch_bounds__(C::NT, C::MIN_BLOCKS) replay_pipe_kernel(const
         if (threadIdx.x == C::NC) producer<C>(p, sm, L, units);
         return;
     }
-    consumer<C>(p, sm, L, units);
+    consumer<C>(p, sm, L);
 }
 
 // ---------------------------------------------------------------------------

@@ -8,7 +8,8 @@ namespace rs {
 
 // ---------------------------------------------------------------- init
 // Writes the fp32 and/or bf16 checkpoint from init (or zeros) and clears the
-// per-sequence pointers, arrival counters and the status word.
+// per-sequence pointers, the arrival and scheduling counters (B + 2) and the
+// status word.
 __global__ void init_kernel(size_t n4, const float4 *init, float4 *hp, uint2 *lp, int B, int32_t *base,
                             int32_t *h, int32_t *nd, uint32_t *arrive, uint32_t *status) {
     const size_t stride = (size_t)gridDim.x * blockDim.x;
@@ -23,7 +24,10 @@ __global__ void init_kernel(size_t n4, const float4 *init, float4 *hp, uint2 *lp
         nd[b] = 0;
         arrive[b] = 0;
     }
-    if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        arrive[B] = arrive[B + 1] = 0;
+        *status = 0;
+    }
 }
 
 cudaError_t init_launch(const rs_layer_desc &d, const rs_state &st, const float *init, cudaStream_t s) {

@@ -46,7 +46,7 @@ class Layer:
         self.base = z(B, torch.int32)
         self.h = z(B, torch.int32)
         self.nd = z(B, torch.int32)
-        self.arrive = z(B, torch.int32)
+        self.arrive = z(sz.arrive // 4, torch.int32)
         self.status_word = z(1, torch.int32)
         p = lambda t: t.data_ptr() if t is not None else None
         self.state = rb.State(p(self.ckpt_hp), p(self.ckpt_lp), p(self.buf_v), p(self.buf_k), p(self.buf_a),
