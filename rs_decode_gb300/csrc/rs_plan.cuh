@@ -85,13 +85,14 @@ __device__ __forceinline__ void arrive_and_update(const ReplayParams &p, const S
     }
 }
 
-// Dynamic unit scheduling.  A launch's units are handed out in order from one
-// counter, arrive[B]: each pipeline takes its next unit when its planner is
-// ready for one, so that a pipeline that drew costly units (a folding unit
-// moves several times the bytes of a streamed one, and which sequences fold
-// depends on their pointers) takes fewer.  The planners finish by counting
-// themselves on arrive[B + 1]; the last one resets both counters for the next
-// launch on the state.
+// Dynamic unit scheduling (the row-split pipeline).  A launch's units are
+// handed out in order from one counter, arrive[B]: each CTA takes its next
+// unit when its producer is ready to plan one, so that a CTA that drew costly
+// units (a folding unit moves twice the bytes of a streamed one, and which
+// sequences fold depends on their pointers) takes fewer.  The producers finish
+// by counting themselves on arrive[B + 1]; the last one resets both counters
+// for the next launch on the state.  (Mamba-2 decode 0.1844 against 0.1876 ms
+// per step with round-robin units, its 4-draft round 0.303 against 0.316 ms.)
 __device__ __forceinline__ int next_unit(const ReplayParams &p) {
     return (int)atomicAdd(p.arrive + p.B, 1u);
 }

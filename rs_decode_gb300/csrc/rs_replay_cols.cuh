@@ -238,8 +238,7 @@ __host__ __device__ inline int pipe_bytes(const RSmem &L) { return (L.total + 10
 // two side by side (2 NT threads, two carve-ups): kernels that hold tensor
 // memory are resident one CTA per SM, so they pair their pipelines in one CTA.
 struct PipeCtx {
-    int u0;                 // the pipeline's index in the grid
-    int planners;           // pipelines in the grid (each plans its own units)
+    int u0, ustride;        // the pipeline's units: u0, u0 + ustride, ...
     int tid;                // thread index within the pipeline
     int bar_prep;           // named barrier of the pipeline's prep warps
     bool tc;                // bf16 blocks are dotted on the tensor cores
@@ -347,12 +346,14 @@ __device__ __forceinline__ void reduce_rows(float (&acc)[WGeo<C, TE>::M], int rg
 }
 
 // ---------------------------------------------------------------------------
-// Planner (one lane of the producer warp): takes the pipeline's next unit from
-// the launch's counter (dynamic scheduling, rs_plan.cuh), reads its pointers,
-// takes part in the pointer update, and hands the plan to the prep warps
-// through a ring of kPlanRing slots, so that the pointer reads and the arrival
-// atomic of later units overlap the prep warps' work on the current one.  A
-// plan with b = -1 ends the pipeline.
+// Planner (one lane of the producer warp): reads each unit's pointers, takes
+// part in the pointer update, and hands the plan to the prep warps through a
+// ring of kPlanRing slots, so that the pointer reads and the arrival atomic of
+// later units overlap the prep warps' work on the current one.  A plan with
+// b = -1 ends the pipeline.  Units are assigned round-robin (u0, u0 + ustride,
+// ...): handing them out from one counter, as the row-split pipeline does,
+// measured slower here (the two-precision GDN round 0.369 against 0.324 ms,
+// same box).
 template <class C>
 __device__ __forceinline__ void planner(const ReplayParams &p, uint8_t *sm, const RSmem &L, int units, int HU,
                                         int NS, const PipeCtx &pc) {
@@ -360,17 +361,12 @@ __device__ __forceinline__ void planner(const ReplayParams &p, uint8_t *sm, cons
     UnitHdr *plans = reinterpret_cast<UnitHdr *>(sm + L.plans);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L.abort);
     const unsigned upseq = p.H / HU;
-    for (int cu = 0;; ++cu) {
+    for (int cu = 0, u = pc.u0;; ++cu, u += pc.ustride) {
         const int slot = cu % kPlanRing;
-        if (!wait_or_abort(pempty + slot, ((cu / kPlanRing) & 1) ^ 1, abort_flag, p.status)) {
-            planner_done(p, pc.planners);
-            return;
-        }
-        const int u = next_unit(p);
+        if (!wait_or_abort(pempty + slot, ((cu / kPlanRing) & 1) ^ 1, abort_flag, p.status)) return;
         if (u >= units) {
             plans[slot].b = -1;
             mbar_arrive(pfull + slot);
-            planner_done(p, pc.planners);
             return;
         }
         const int b = u / upseq;
@@ -722,14 +718,66 @@ __device__ __forceinline__ bool kda_scan(const ReplayParams &p, uint8_t *cx, con
     float *fw = reinterpret_cast<float *>(cx + L.fw), *gF = reinterpret_cast<float *>(cx + L.gF);
     float *qs = reinterpret_cast<float *>(cx + L.qs);
     float *gv = reinterpret_cast<float *>(cx + L.gv), *fk = reinterpret_cast<float *>(cx + L.fk);
-    for (int hd = pw; hd < HU; hd += C::NPW) {
-        const int hh = h0 + hd;
+    // Warps per head: with one head per unit (and up to three drafts, whose
+    // exchange below fits the head's fold-key area) the three prep warps split
+    // the records into contiguous chunks, the highest first; each first forms
+    // its chunk's products per bound, takes the products of the chunks above
+    // it from the others, then scans its chunk.  Otherwise one warp per head.
+    constexpr bool SPLIT = TMAX <= 3;
+    const int wph = (SPLIT && HU < C::NPW) ? C::NPW / HU : 1;
+    const int per = (nrec + wph - 1) / wph;
+    for (int task = pw; task < (wph > 1 ? HU * wph : HU); task += (wph > 1 ? HU * wph : C::NPW)) {
+        const int hd = task % HU, ci = task / HU, hh = h0 + hd;
+        const int hi = nrec - ci * per > 0 ? nrec - ci * per : 0, lo = hi - per > 0 ? hi - per : 0;
         float Pd[TMAX][NPL], PF[NPL];  // running products: prod_{s=r+1..m} alpha_s[n]
 #pragma unroll
         for (int t = 0; t < NPL; ++t) {
             PF[t] = 1.f;
 #pragma unroll
             for (int i = 0; i < TMAX; ++i) Pd[i][t] = 1.f;
+        }
+        auto alpha_src = [&](int r) {
+            return r < hc ? p.buf_a + (((size_t)b * cap + slot(r)) * H + hh) * N
+                          : p.alpha + (((size_t)b * T + (r - hc)) * H + hh) * N;
+        };
+        if (SPLIT && wph > 1) {
+            // pass 1: this chunk's products per bound, exchanged through the
+            // head's fold-key area [chunk][bound][N] (pass 2 writes it later)
+            float Qd[SPLIT ? TMAX : 1][NPL], QF[NPL];
+#pragma unroll
+            for (int t = 0; t < NPL; ++t) {
+                QF[t] = 1.f;
+#pragma unroll
+                for (int i = 0; i < TMAX; ++i) Qd[i][t] = 1.f;
+            }
+            for (int r = lo; r < hi; ++r) {
+                const float *asrc = alpha_src(r);
+#pragma unroll
+                for (int t = 0; t < NPL; ++t) {
+                    const float a = asrc[lane + 32 * t];
+#pragma unroll
+                    for (int i = 0; i < TMAX; ++i)
+                        if (i < T && r <= hc + i) Qd[i][t] *= a;
+                    if (r < F) QF[t] *= a;
+                }
+            }
+            float *xq = fk + (size_t)hd * cap * N;
+#pragma unroll
+            for (int t = 0; t < NPL; ++t) {
+#pragma unroll
+                for (int i = 0; i < TMAX; ++i) xq[((size_t)ci * (TMAX + 1) + i) * N + lane + 32 * t] = Qd[i][t];
+                xq[((size_t)ci * (TMAX + 1) + TMAX) * N + lane + 32 * t] = QF[t];
+            }
+            if (named_sync_or(pc.bar_prep, C::NPT, false)) return false;
+            for (int c2i = 0; c2i < ci; ++c2i) {  // the chunks above this one
+#pragma unroll
+                for (int t = 0; t < NPL; ++t) {
+#pragma unroll
+                    for (int i = 0; i < TMAX; ++i) Pd[i][t] *= xq[((size_t)c2i * (TMAX + 1) + i) * N + lane + 32 * t];
+                    PF[t] *= xq[((size_t)c2i * (TMAX + 1) + TMAX) * N + lane + 32 * t];
+                }
+            }
+            if (named_sync_or(pc.bar_prep, C::NPT, false)) return false;  // read before pass 2 writes fk
         }
         // the drafts' keys and queries at the lane's channels, read once (up to
         // four drafts; more are read per record)
@@ -746,15 +794,14 @@ __device__ __forceinline__ bool kda_scan(const ReplayParams &p, uint8_t *cx, con
         }
         // the records' decay vectors are loaded CA records at a time, ahead of
         // their use (they come from L2 or HBM; the scan is sequential)
-        constexpr int CA = TMAX <= 4 ? 8 : 4;
-        for (int rc = nrec - 1; rc >= 0; rc -= CA) {
+        constexpr int CA = TMAX <= 3 ? 8 : 4;
+        for (int rc = hi - 1; rc >= lo; rc -= CA) {
             float ac[CA][NPL];
 #pragma unroll
             for (int q = 0; q < CA; ++q) {
                 const int r = rc - q;
-                if (r >= 0) {
-                    const float *asrc = r < hc ? p.buf_a + (((size_t)b * cap + slot(r)) * H + hh) * N
-                                               : p.alpha + (((size_t)b * T + (r - hc)) * H + hh) * N;
+                if (r >= lo) {
+                    const float *asrc = alpha_src(r);
 #pragma unroll
                     for (int t = 0; t < NPL; ++t) ac[q][t] = asrc[lane + 32 * t];
                 }
@@ -762,7 +809,7 @@ __device__ __forceinline__ bool kda_scan(const ReplayParams &p, uint8_t *cx, con
 #pragma unroll
         for (int q = 0; q < CA; ++q) {
             const int r = rc - q;
-            if (r < 0) break;
+            if (r < lo) break;
             float a[NPL], kr[NPL];
 #pragma unroll
             for (int t = 0; t < NPL; ++t) {
@@ -813,7 +860,8 @@ __device__ __forceinline__ bool kda_scan(const ReplayParams &p, uint8_t *cx, con
             }
         }
         }
-        // the running products are now gamma(m_i) and gamma(F - 1)
+        // the warp whose chunk ends at record 0 now holds gamma(m_i) and gamma(F - 1)
+        if (lo != 0 || (hi == 0 && ci != 0)) continue;
         float *qh = qs + (size_t)hd * N * JP;
 #pragma unroll
         for (int t = 0; t < NPL; ++t) {
@@ -1529,7 +1577,7 @@ __global__ void __launch_bounds__(C::NT * PIPES, PIPES == 1 ? C::MIN_BLOCKS : 1)
     uint8_t *sm = sm0 + (size_t)pipe * pipe_bytes(L);
     PipeCtx pc;
     pc.u0 = blockIdx.x * PIPES + pipe;
-    pc.planners = gridDim.x * PIPES;
+    pc.ustride = gridDim.x * PIPES;
     pc.tid = threadIdx.x & (C::NT - 1);
     pc.bar_prep = 1 + pipe;  // named barriers 1 .. PIPES; PIPES + 1: every consumer warp of the CTA
     pc.tc = TC;
