@@ -438,8 +438,7 @@ struct FoldSrc {
 
 // Gathers fw_r v_r[p] for records r0 .. r0+nr-1 and the warp's WC = P/NCW
 // value columns (from column wcol0 on) into the warp's scratch
-// cfs[r - r0][WC], fp32.  The loads of a chunk are independent and issued
-// together.
+// cfs[r - r0][WC], fp32.  The loads of a chunk are independent.
 template <class C>
 __device__ __forceinline__ void gather_fold_coefs(float *cfs, const FoldSrc &fs, const float *fw, int r0, int nr,
                                                   int j, int wcol0, int lane) {
@@ -460,6 +459,33 @@ __device__ __forceinline__ void gather_fold_coefs(float *cfs, const FoldSrc &fs,
         *reinterpret_cast<float4 *>(cfs + (r - r0) * WC + 4 * c4) =
             make_float4(w * v[0], w * v[1], w * v[2], w * v[3]);
     }
+    __syncwarp();
+}
+
+// As gather_fold_coefs for fp32 records (GDN, KDA), without the factor fw_r
+// (the caller applies it as it reads): the committed records' u go straight
+// from global memory to the scratch with cp.async, all of a lane's copies in
+// flight at once and no registers held; this launch's records (in shared
+// memory) are copied directly.
+template <class C>
+__device__ __forceinline__ void gather_fold_values_async(float *cfs, const FoldSrc &fs, int nr, int wcol0,
+                                                         int lane) {
+    static_assert(C::KIND != RS_MAMBA2, "fp32 record values");
+    constexpr int WC = C::P / C::NCW, Q = WC / 4;
+    __syncwarp();  // the previous coefficients have been read
+    for (int i = lane; i < nr * Q; i += 32) {
+        const int r = i / Q, c4 = i % Q;
+        float *dst = cfs + r * WC + 4 * c4;
+        if (r < fs.hc) {
+            int sl = fs.base + r;
+            if (sl >= fs.cap) sl -= fs.cap;
+            cp_async16(dst, fs.committed + (size_t)sl * fs.slot_stride + (size_t)(wcol0 + 4 * c4) * 4);
+        } else {
+            *reinterpret_cast<float4 *>(dst) = *reinterpret_cast<const float4 *>(
+                fs.fresh + (size_t)(r - fs.hc) * fs.fresh_stride + (size_t)(wcol0 + 4 * c4) * 4);
+        }
+    }
+    cp_async_wait_all();
     __syncwarp();
 }
 
@@ -568,7 +594,7 @@ __device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages
             // lanes of a shared-memory phase still read one whole line; the
             // line's swizzle phase alternates with the row (NCB lines per row).
             const int cg = lane & 7, rg = lane >> 3, cb = wcol0 / W::CBE;
-            gather_fold_coefs<C>(cfs, fs, fw, 0, F > 0 ? F : 0, j, wcol0, lane);
+            gather_fold_values_async<C>(cfs, fs, F > 0 ? F : 0, wcol0, lane);
             for (int rb = 0; rb < NCB; ++rb) {
                 const uint8_t *sb = stages + (size_t)ring_add(q0, rb, NS).s * C::STAGE;
                 float o[8][4];
@@ -585,6 +611,9 @@ __device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages
                 for (int r = 0; r < F; ++r) {
                     float cf[4], kv[8];
                     load_f32_vec<4>(cfs + r * (C::P / C::NCW) + lcol, cf);
+                    const float w = fw[j * fs.cap + r];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) cf[e] *= w;
                     if constexpr (C::KDA) load_f32_vec<8>(fkh + (size_t)r * C::N + rb * RB + 8 * rg, kv);
                     else unpack<uint16_t, 8>(ld_u4(kr + (size_t)r * C::N), kv);
 #pragma unroll
@@ -930,6 +959,16 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
 #pragma unroll
     for (int t = 0; t < 8; ++t) xv[t] = x_task && t < nrec ? ld_u4(x_src(t)) : make_uint4(0u, 0u, 0u, 0u);
 
+    // GDN, KDA: the committed records' u (P fp32 per head and record) are read
+    // by the consumer warps (the record parts of the outputs, and the fold's
+    // coefficients) one unit later; bring their lines into L2 now
+    if (C::DELTA && T > 0) {
+        constexpr int LPU = P * 4 / 128;  // 128-byte lines per record value
+        for (int i2 = tp; i2 < HU * hc * LPU; i2 += NPT) {
+            const int l = i2 % LPU, r = (i2 / LPU) % hc, hh = h0 + i2 / (LPU * hc);
+            prefetch_l2(static_cast<const float *>(p.buf_v) + (((size_t)b * cap + slot(r)) * H + hh) * P + l * 32);
+        }
+    }
     // KDA: the records' decay vectors (N fp32 per head and record) are read by
     // the sequential scan; bring their lines into L2 now, so that they arrive
     // while the staging below waits
