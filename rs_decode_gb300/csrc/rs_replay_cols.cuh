@@ -945,19 +945,22 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
     float *pre1 = reinterpret_cast<float *>(cx + L.pre1);
     float *qs = reinterpret_cast<float *>(cx + L.qs);
 
-    // Mamba-2 step-5 task of this thread (one head, 8 value columns): the first
-    // 8 records' x are loaded now, so that their latency overlaps the staging
+    // Mamba-2 step-5 tasks: one head, 8 value columns and a group of XDG drafts
+    // (all drafts at once would leave most prep threads idle at two heads per
+    // unit).  The first task's first 8 records' x are loaded now, so that their
+    // latency overlaps the staging.
     constexpr int PC8 = P / 8;
-    const int x_hd = tp / PC8, x_pc = tp % PC8;
-    const bool x_task = KIND == RS_MAMBA2 && T > 0 && x_hd < HU;
+    constexpr int XDG = TMAX >= 4 ? 2 : TMAX, XNG = TMAX / XDG;  // drafts per task, draft groups
+    const int x_tasks = KIND == RS_MAMBA2 && T > 0 ? HU * PC8 * XNG : 0;
     const uint16_t *xbuf = static_cast<const uint16_t *>(p.buf_v);
-    auto x_src = [&](int r) {
-        return (r < hc ? xbuf + (((size_t)b * cap + slot(r)) * H + h0 + x_hd) * P
-                       : p.x + (((size_t)b * T + (r - hc)) * H + h0 + x_hd) * P) + 8 * x_pc;
+    auto x_src = [&](int task, int r) {
+        const int hd = (task / PC8) % HU, pc = task % PC8;
+        return (r < hc ? xbuf + (((size_t)b * cap + slot(r)) * H + h0 + hd) * P
+                       : p.x + (((size_t)b * T + (r - hc)) * H + h0 + hd) * P) + 8 * pc;
     };
     uint4 xv[8];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) xv[t] = x_task && t < nrec ? ld_u4(x_src(t)) : make_uint4(0u, 0u, 0u, 0u);
+    for (int t = 0; t < 8; ++t) xv[t] = tp < x_tasks && t < nrec ? ld_u4(x_src(tp, t)) : make_uint4(0u, 0u, 0u, 0u);
 
     // GDN, KDA: the committed records' u (P fp32 per head and record) are read
     // by the consumer warps (the record parts of the outputs, and the fold's
@@ -1211,48 +1214,50 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
     // ---- 5. the parts of the outputs that come from the records, per value column
     if (KIND == RS_MAMBA2 && T > 0) {
         // rec_i[p] = sum_{r <= m_i} c1[i][r] x_r[p] + D x_{m_i}[p]: one task per
-        // head and 8 columns, all drafts at once; the records' x come from
-        // global memory, 8 records' loads in flight at a time (the first 8
-        // were issued before the staging).  The task also appends the new x.
-        if (x_task) {
-            const int hd = x_hd, pc = x_pc;
+        // head, 8 columns and XDG drafts; the records' x come from global
+        // memory, 8 records' loads in flight at a time (the first task's first
+        // 8 were issued before the staging).  The tasks of the first draft
+        // group also append the new x.
+        for (int task = tp; task < x_tasks; task += NPT) {
+            const int pc = task % PC8, hd = (task / PC8) % HU, ig = task / (PC8 * HU), i0 = ig * XDG;
             const float d = cst[HU + hd];
-            float a[TMAX][8];
+            float a[XDG][8];
 #pragma unroll
-            for (int i = 0; i < TMAX; ++i)
+            for (int i = 0; i < XDG; ++i)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) a[i][e] = 0.f;
             for (int r0 = 0; r0 < nrec; r0 += 8) {
-                if (r0 > 0) {
+                if (r0 > 0 || task != tp) {
 #pragma unroll
                     for (int t = 0; t < 8; ++t)
-                        xv[t] = r0 + t < nrec ? ld_u4(x_src(r0 + t)) : make_uint4(0u, 0u, 0u, 0u);
+                        xv[t] = r0 + t < nrec ? ld_u4(x_src(task, r0 + t)) : make_uint4(0u, 0u, 0u, 0u);
                 }
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
                     const int r = r0 + t;
                     if (r >= nrec) break;
-                    if (append && r >= hc)
+                    if (append && r >= hc && ig == 0)
                         *reinterpret_cast<uint4 *>(const_cast<uint16_t *>(xbuf) +
                                                    (((size_t)b * cap + slot(r)) * H + h0 + hd) * P + 8 * pc) = xv[t];
                     float xf[8];
                     unpack<uint16_t, 8>(xv[t], xf);
 #pragma unroll
-                    for (int i = 0; i < TMAX; ++i) {
+                    for (int k = 0; k < XDG; ++k) {
+                        const int i = i0 + k;
                         if (i < T && r <= hc + i) {
                             const float c = c1[(hd * TMAX + i) * cap + r] + (r == hc + i ? d : 0.f);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) a[i][e] = fmaf(c, xf[e], a[i][e]);
+                            for (int e = 0; e < 8; ++e) a[k][e] = fmaf(c, xf[e], a[k][e]);
                         }
                     }
                 }
             }
 #pragma unroll
-            for (int i = 0; i < TMAX; ++i) {
-                if (i < T) {
-                    float4 *dst = reinterpret_cast<float4 *>(pre1 + (hd * TMAX + i) * P + 8 * pc);
-                    dst[0] = make_float4(a[i][0], a[i][1], a[i][2], a[i][3]);
-                    dst[1] = make_float4(a[i][4], a[i][5], a[i][6], a[i][7]);
+            for (int k = 0; k < XDG; ++k) {
+                if (i0 + k < T) {
+                    float4 *dst = reinterpret_cast<float4 *>(pre1 + (hd * TMAX + i0 + k) * P + 8 * pc);
+                    dst[0] = make_float4(a[k][0], a[k][1], a[k][2], a[k][3]);
+                    dst[1] = make_float4(a[k][4], a[k][5], a[k][6], a[k][7]);
                 }
             }
         }
