@@ -310,7 +310,7 @@ def measure_decode(w, K, W, dev, rank, world, want_eager=True, want_e2e=True, wa
     npool = min(INPUT_POOL, K + W)
     host_steps = [synth.step_inputs(w, s, seed=rank_seed(rank), params=params) for s in range(npool)]
     dev_steps = [to_device(d, dev) for d in host_steps]
-    prec = {"fp32": rb.PREC_FP32, "two": rb.PREC_TWO, "shared_bf16": rb.PREC_SHARED_BF16}[w.precision]
+    prec = rb.PRECISIONS[w.precision]
     layer = Layer(w.kind, w.B, w.H, w.G, w.P, w.N, w.L, capacity=w.cap, precision=prec)
     S0 = _init_state(layer, w, dev, rank)
     y = torch.empty(w.B, w.H, w.P, device=dev)
@@ -356,9 +356,9 @@ def measure_decode(w, K, W, dev, rank, world, want_eager=True, want_e2e=True, wa
         raise RuntimeError("device status bits set during the benchmark")
 
     # algorithmic bytes of the timed launches (the pointer schedule is lockstep)
-    shape = traffic.Shape(w.kind, w.B, w.H, w.G, w.P, w.N)
+    shape = traffic.Shape(w.kind, w.B, w.H, w.G, w.P, w.N, u_bytes=2 if "u16" in w.precision else 4)
     total_bytes, h = 0, h0
-    two = w.precision == "two"
+    two = w.precision.startswith("two")
     per_launch = []  # (folds, bytes, ms) of every timed launch
     for s in range(K):
         flush = h + 1 >= w.L
@@ -488,7 +488,7 @@ def measure_spec(w, rounds, W, dev, rank):
     npool = 32
     host = [synth.round_inputs(w, r, seed=rank_seed(rank), params=params) for r in range(npool)]
     dev_rounds = [to_device(d, dev) for d in host]
-    prec = {"fp32": rb.PREC_FP32, "two": rb.PREC_TWO, "shared_bf16": rb.PREC_SHARED_BF16}[w.precision]
+    prec = rb.PRECISIONS[w.precision]
     layer = Layer(w.kind, w.B, w.H, w.G, w.P, w.N, w.L, T_max=w.T, capacity=w.cap, precision=prec)
     y = torch.empty(w.B, w.T, w.H, w.P, device=dev)
     stream = torch.cuda.current_stream()
@@ -518,8 +518,8 @@ def measure_spec(w, rounds, W, dev, rank):
     ms = e0.elapsed_time(e1) / rounds
     if layer.status() != 0:
         raise RuntimeError("device status bits set during the speculative benchmark")
-    shape = traffic.Shape(w.kind, w.B, w.H, w.G, w.P, w.N)
-    two = w.precision == "two"
+    shape = traffic.Shape(w.kind, w.B, w.H, w.G, w.P, w.N, u_bytes=2 if "u16" in w.precision else 4)
+    two = w.precision.startswith("two")
     tot_bytes, folds, committed = 0, 0, 0
     for r in range(W, W + rounds):
         for hb in h_before[r]:
@@ -593,6 +593,13 @@ def run_sweeps(dev):
         print(json.dumps({"sweep": "batch", "L": 16, "B": B, **dec(base.with_(B=B))}), flush=True)
     print(json.dumps({"sweep": "precision", "precision": "two", "B": 256, "L": 16,
                       **dec(base.with_(precision="two"))}), flush=True)
+    gdn = synth.WORKLOADS["gdn"]
+    for prec in ("fp32", "fp32+u16"):  # GDN records with u in fp32 or bf16
+        m = measure_decode(gdn.with_(precision=prec), 256, 2 * gdn.L, dev, 0, 1, want_e2e=False, want_clocks=False)
+        gbs = m["bytes_per_launch"] / (m["ms_per_step"] * 1e-3) / 1e9
+        print(json.dumps({"sweep": "gdn records", "precision": prec, "B": 256, "L": 16,
+                          "tokens_per_s": gdn.B / (m["ms_per_step"] * 1e-3), "bytes_per_step": m["bytes_per_launch"],
+                          "achieved_gbs": gbs, "frac": gbs / peak}), flush=True)
     spec = synth.WORKLOADS["mamba2_spec"]
     for T in (1, 2, 4, 8):
         o = measure_spec(spec.with_(T=T, capacity=16 + T), 64, 8, dev, 0)

@@ -94,6 +94,14 @@ typedef enum {
  * u_t = beta_t (v_t - D_t k_t), S_t = D_t + u_t k_t^T, y_t = S_t q_t. */
 typedef enum { RS_MAMBA2 = 0, RS_GDN = 1, RS_KDA = 2 } rs_kind;
 
+/* Flag OR-ed into rs_layer_desc.precision: Gated DeltaNet records keep the
+ * correction term u in bf16 (round to nearest even) instead of fp32, halving
+ * the records' value bytes.  Outputs and folds then read rounded u: their
+ * error bound is that of values read from bf16 (a measured variant; the
+ * pages are silent on the buffer's precision).  RS_GDN only.
+ * Source: [CSI] "How it works", Gated DeltaNet bullet (records store u). */
+#define RS_U_BF16 0x10
+
 typedef enum {
     RS_PREC_FP32 = 0,        /* fp32 checkpoint only                                          */
     RS_PREC_TWO = 1,         /* fp32 high-precision copy + bf16 low-precision copy: non-flush
@@ -117,7 +125,7 @@ typedef struct {
     int32_t L;         /* window: a standard step flushes when it makes h >= L */
     int32_t T_max;     /* largest draft count of rs_verify (0: standard only)  */
     int32_t capacity;  /* circular buffer slots per sequence                   */
-    int32_t precision; /* rs_precision                                         */
+    int32_t precision; /* rs_precision, optionally | RS_U_BF16 (GDN)          */
 } rs_layer_desc;
 
 /* Per-layer state; every member is a caller-allocated device array. */
@@ -125,7 +133,8 @@ typedef struct {
     float *ckpt_hp;    /* fp32 checkpoint [B][H][N][P]; NULL for RS_PREC_SHARED_BF16 */
     uint16_t *ckpt_lp; /* bf16 checkpoint [B][H][N][P]; NULL for RS_PREC_FP32        */
     void *buf_v;       /* records' values: Mamba-2 x bf16 [B][cap][H][P];
-                          GDN / KDA correction term u fp32 [B][cap][H][P]             */
+                          GDN / KDA correction term u fp32 [B][cap][H][P]
+                          (bf16 with RS_U_BF16)                                       */
     uint16_t *buf_k;   /* records' keys (Mamba-2 B / GDN k) bf16 [B][cap][G][N]       */
     float *buf_a;      /* records' decays alpha, fp32 [B][cap][H] (Mamba-2: exp(dt A));
                           KDA [B][cap][H][N]                                          */

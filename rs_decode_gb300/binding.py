@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(HERE, "librs.so")
 
 MAMBA2, GDN, KDA = 0, 1, 2
 PREC_FP32, PREC_TWO, PREC_SHARED_BF16 = 0, 1, 2
+U_BF16 = 0x10  # flag: GDN records keep u in bf16
 DEV_CAPACITY, DEV_ACCEPT, DEV_DRAFTS_PENDING = 0x1, 0x2, 0x4
 STATUS = {0: "RS_OK", 1: "RS_ERR_INVALID_ARG", 2: "RS_ERR_UNSUPPORTED", 3: "RS_ERR_CAPACITY",
           4: "RS_ERR_CUDA", 5: "RS_ERR_DEVICE", 6: "RS_ERR_STATIC_LIMIT"}
@@ -132,6 +133,12 @@ def _check(fn: str, status: int) -> None:
 def make_desc(kind: int, B: int, H: int, G: int, P: int, N: int, L: int, T_max: int = 0,
               capacity: int | None = None, precision: int = PREC_FP32) -> LayerDesc:
     return LayerDesc(kind, B, H, G, P, N, L, T_max, capacity if capacity else max(L, T_max) + T_max, precision)
+
+
+# Precision names of the synthetic workloads: the checkpoint's, and "+u16"
+# for GDN records that keep u in bf16.
+PRECISIONS = {"fp32": PREC_FP32, "two": PREC_TWO, "shared_bf16": PREC_SHARED_BF16,
+              "fp32+u16": PREC_FP32 | U_BF16, "two+u16": PREC_TWO | U_BF16}
 
 
 def make_inputs(**tensors) -> Inputs:

@@ -33,7 +33,8 @@ rs_status check_desc(const rs_layer_desc *d) {
     // slabs of the smallest shape (64 x 64 bf16) are already 512 GiB
     if ((long long)d->B * d->H > kMaxSlabs) return RS_ERR_INVALID_ARG;
     if (d->P < 1 || d->N < 1 || d->L < 1 || d->T_max < 0 || d->T_max > kMaxT) return RS_ERR_INVALID_ARG;
-    if (d->precision < RS_PREC_FP32 || d->precision > RS_PREC_SHARED_BF16) return RS_ERR_INVALID_ARG;
+    const int ckpt = d->precision & ~RS_U_BF16;
+    if (ckpt < RS_PREC_FP32 || ckpt > RS_PREC_SHARED_BF16) return RS_ERR_INVALID_ARG;
     if (d->capacity > kMaxCap || d->capacity < 1) return RS_ERR_INVALID_ARG;
     // A standard step needs the h <= L - 1 records since the checkpoint plus
     // its own; a round of T drafts needs h + T, and after a fully accepted
@@ -43,12 +44,14 @@ rs_status check_desc(const rs_layer_desc *d) {
     if (d->capacity < (d->L > d->T_max ? d->L : d->T_max) + d->T_max) return RS_ERR_CAPACITY;
     if (!replay_shape_supported(d->kind, d->P, d->N)) return RS_ERR_UNSUPPORTED;
     if (d->kind == RS_KDA && d->precision != RS_PREC_FP32) return RS_ERR_UNSUPPORTED;
+    if ((d->precision & RS_U_BF16) && d->kind != RS_GDN) return RS_ERR_UNSUPPORTED;
     return RS_OK;
 }
 
 rs_status check_state(const rs_layer_desc *d, const rs_state *s, bool need_arrive) {
     if (!s) return RS_ERR_INVALID_ARG;
-    const bool need_hp = d->precision != RS_PREC_SHARED_BF16, need_lp = d->precision != RS_PREC_FP32;
+    const int ckpt = d->precision & ~RS_U_BF16;
+    const bool need_hp = ckpt != RS_PREC_SHARED_BF16, need_lp = ckpt != RS_PREC_FP32;
     if (need_hp != (s->ckpt_hp != nullptr) || need_lp != (s->ckpt_lp != nullptr)) return RS_ERR_INVALID_ARG;
     if (need_hp && !aligned(s->ckpt_hp, 16)) return RS_ERR_INVALID_ARG;
     if (need_lp && !aligned(s->ckpt_lp, 16)) return RS_ERR_INVALID_ARG;
@@ -93,7 +96,7 @@ namespace {
 ReplayParams replay_params(const rs_layer_desc *d, const rs_state *s, int mode, int T) {
     ReplayParams p = {};
     p.B = d->B; p.H = d->H; p.G = d->G; p.L = d->L; p.cap = d->capacity; p.T = T;
-    p.prec = d->precision; p.mode = mode;
+    p.prec = d->precision & ~RS_U_BF16; p.u16 = (d->precision & RS_U_BF16) != 0; p.mode = mode;
     p.ckpt_hp = s->ckpt_hp; p.ckpt_lp = s->ckpt_lp;
     p.buf_v = s->buf_v; p.buf_k = s->buf_k; p.buf_a = s->buf_a; p.buf_s = s->buf_s;
     p.base = s->base; p.h = s->h; p.nd = s->nd; p.arrive = s->arrive; p.status = s->status;
@@ -137,9 +140,10 @@ rs_status rs_state_bytes_for(const rs_layer_desc *d, rs_state_bytes *o) {
     RS_TRY(check_desc(d));
     if (!o) return RS_ERR_INVALID_ARG;
     const size_t B = d->B, H = d->H, G = d->G, P = d->P, N = d->N, C = d->capacity;
-    o->ckpt_hp = d->precision != RS_PREC_SHARED_BF16 ? B * H * N * P * 4 : 0;
-    o->ckpt_lp = d->precision != RS_PREC_FP32 ? B * H * N * P * 2 : 0;
-    o->buf_v = B * C * H * P * (d->kind == RS_MAMBA2 ? 2 : 4);
+    const int ckpt = d->precision & ~RS_U_BF16;
+    o->ckpt_hp = ckpt != RS_PREC_SHARED_BF16 ? B * H * N * P * 4 : 0;
+    o->ckpt_lp = ckpt != RS_PREC_FP32 ? B * H * N * P * 2 : 0;
+    o->buf_v = B * C * H * P * (d->kind == RS_MAMBA2 || (d->precision & RS_U_BF16) ? 2 : 4);
     o->buf_k = B * C * G * N * 2;
     o->buf_a = B * C * H * (d->kind == RS_KDA ? N : 1) * 4;
     o->buf_s = d->kind == RS_MAMBA2 ? B * C * H * 4 : 0;

@@ -53,6 +53,7 @@ rs_status cuda_status(cudaError_t e);
 // Arguments of the replay kernels (decode, verify, flush, materialise).
 struct ReplayParams {
     int B, H, G, L, cap, T, prec, mode;
+    int u16;     // GDN records keep u in bf16 (RS_U_BF16)
     float *ckpt_hp;
     uint16_t *ckpt_lp;
     void *buf_v;

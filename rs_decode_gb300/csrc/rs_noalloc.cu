@@ -122,7 +122,7 @@ extern "C" rs_status rs_decode_mamba2_noalloc(const rs_layer_desc *d, const rs_s
 
     rs::ReplayParams p = {};
     p.B = d->B; p.H = d->H; p.G = d->G; p.L = d->L; p.cap = d->capacity; p.T = 1;
-    p.prec = d->precision; p.mode = rs::MODE_DECODE;
+    p.prec = d->precision; p.u16 = 0; p.mode = rs::MODE_DECODE;  // (Mamba-2: no flag)
     p.ckpt_hp = st->ckpt_hp; p.ckpt_lp = st->ckpt_lp;
     p.buf_v = st->buf_v; p.buf_k = st->buf_k; p.buf_a = st->buf_a; p.buf_s = st->buf_s;
     p.base = st->base; p.h = st->h; p.nd = st->nd; p.arrive = arrive; p.status = st->status;

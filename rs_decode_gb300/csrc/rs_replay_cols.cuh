@@ -434,6 +434,7 @@ struct FoldSrc {
     const uint8_t *fresh;      // record hc of this (sequence, head)
     size_t slot_stride, fresh_stride;  // bytes between slots / between this launch's records
     int base, hc, cap;
+    int u16;                   // GDN: the committed records keep u in bf16 (this launch's are fp32)
 };
 
 // Gathers fw_r v_r[p] for records r0 .. r0+nr-1 and the warp's WC = P/NCW
@@ -449,13 +450,15 @@ __device__ __forceinline__ void gather_fold_coefs(float *cfs, const FoldSrc &fs,
         const int r = r0 + i / Q, c4 = i % Q;
         int sl = fs.base + r;
         if (sl >= fs.cap) sl -= fs.cap;
+        // Mamba-2 x is bf16 throughout; GDN u is fp32, or bf16 in the buffer with RS_U_BF16
+        const bool b16 = C::KIND == RS_MAMBA2 || (fs.u16 && r < fs.hc);
         const uint8_t *src = (r < fs.hc ? fs.committed + (size_t)sl * fs.slot_stride
                                         : fs.fresh + (size_t)(r - fs.hc) * fs.fresh_stride) +
-                             (size_t)(wcol0 + 4 * c4) * VSZ;
+                             (size_t)(wcol0 + 4 * c4) * (b16 ? 2 : VSZ);
         float v[4];
-        if constexpr (C::KIND == RS_MAMBA2) load_bf16_vec<4>(reinterpret_cast<const uint16_t *>(src), v);
+        if (b16) load_bf16_vec<4>(reinterpret_cast<const uint16_t *>(src), v);
         else load_f32_vec<4>(reinterpret_cast<const float *>(src), v);
-        const float w = fw[j * fs.cap + r];
+        const float w = fw ? fw[j * fs.cap + r] : 1.f;
         *reinterpret_cast<float4 *>(cfs + (r - r0) * WC + 4 * c4) =
             make_float4(w * v[0], w * v[1], w * v[2], w * v[3]);
     }
@@ -594,7 +597,8 @@ __device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages
             // lanes of a shared-memory phase still read one whole line; the
             // line's swizzle phase alternates with the row (NCB lines per row).
             const int cg = lane & 7, rg = lane >> 3, cb = wcol0 / W::CBE;
-            gather_fold_values_async<C>(cfs, fs, F > 0 ? F : 0, wcol0, lane);
+            if (fs.u16) gather_fold_coefs<C>(cfs, fs, nullptr, 0, F > 0 ? F : 0, j, wcol0, lane);
+            else gather_fold_values_async<C>(cfs, fs, F > 0 ? F : 0, wcol0, lane);
             for (int rb = 0; rb < NCB; ++rb) {
                 const uint8_t *sb = stages + (size_t)ring_add(q0, rb, NS).s * C::STAGE;
                 float o[8][4];
@@ -966,10 +970,10 @@ __device__ __forceinline__ bool prep_unit(const ReplayParams &p, uint8_t *sm, co
     // by the consumer warps (the record parts of the outputs, and the fold's
     // coefficients) one unit later; bring their lines into L2 now
     if (C::DELTA && T > 0) {
-        constexpr int LPU = P * 4 / 128;  // 128-byte lines per record value
-        for (int i2 = tp; i2 < HU * hc * LPU; i2 += NPT) {
-            const int l = i2 % LPU, r = (i2 / LPU) % hc, hh = h0 + i2 / (LPU * hc);
-            prefetch_l2(static_cast<const float *>(p.buf_v) + (((size_t)b * cap + slot(r)) * H + hh) * P + l * 32);
+        const int esz = p.u16 ? 2 : 4, lpu = P * esz / 128;  // 128-byte lines per record value
+        for (int i2 = tp; i2 < HU * hc * lpu; i2 += NPT) {
+            const int l = i2 % lpu, r = (i2 / lpu) % hc, hh = h0 + i2 / (lpu * hc);
+            prefetch_l2(static_cast<const uint8_t *>(p.buf_v) + ((((size_t)b * cap + slot(r)) * H + hh) * P) * esz + l * 128);
         }
     }
     // KDA: the records' decay vectors (N fp32 per head and record) are read by
@@ -1326,7 +1330,6 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
     const bool hold = NPASS > 1 || keep;
     const uint8_t *stages = sm + L.stages;
     bool ok = true;
-    constexpr int VSZ = KIND == RS_MAMBA2 ? 2 : 4;
     Ring q0 = it;  // the head's first row block
     for (int j = 0; j < HU && ok; ++j, q0 = ring_add(q0, NCB, NS)) {
         const int hh = h0 + j;
@@ -1336,8 +1339,10 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
         const float *gvh = C::KDA ? gv + (size_t)j * N : nullptr;
         const float *fkh = C::KDA ? fk + (size_t)j * cap * N : nullptr;
         FoldSrc fs;
-        fs.committed = static_cast<const uint8_t *>(p.buf_v) + ((size_t)b * cap * H + hh) * P * VSZ;
-        fs.slot_stride = (size_t)H * P * VSZ;
+        const int csz = (KIND == RS_MAMBA2 || p.u16) ? 2 : 4;  // bytes per buffered value
+        fs.committed = static_cast<const uint8_t *>(p.buf_v) + ((size_t)b * cap * H + hh) * P * csz;
+        fs.slot_stride = (size_t)H * P * csz;
+        fs.u16 = KIND != RS_MAMBA2 && p.u16;
         if (KIND == RS_MAMBA2) {
             fs.fresh = reinterpret_cast<const uint8_t *>(p.x) + ((size_t)b * T * H + hh) * P * 2;
             fs.fresh_stride = (size_t)H * P * 2;
@@ -1397,11 +1402,15 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
             // the dots (the tensor cores' or the lane's own).
             constexpr int UPF = 8;
             const int pl = (TC && C::UMMA && sizeof(TE) == 2) ? 32 * warp + lane : col0 + (rg >> (LR - ilog2(VEC)));
-            const float *ucol = static_cast<const float *>(p.buf_v) + ((size_t)b * cap * H + hh) * P + pl;
-            const size_t ustride = (size_t)H * P;
+            const size_t uoff = ((size_t)b * cap * H + hh) * P + pl, ustride = (size_t)H * P;
+            const bool u16 = p.u16 != 0;
+            auto u_at = [&](int r) {  // committed record r's u at the lane's column
+                const size_t i = uoff + slot(r) * ustride;
+                return u16 ? bf2f(static_cast<const uint16_t *>(p.buf_v)[i]) : static_cast<const float *>(p.buf_v)[i];
+            };
             float upf[UPF];
 #pragma unroll
-            for (int t = 0; t < UPF; ++t) upf[t] = t < hc ? ucol[slot(t) * ustride] : 0.f;
+            for (int t = 0; t < UPF; ++t) upf[t] = t < hc ? u_at(t) : 0.f;
             if constexpr (TC && C::UMMA && sizeof(TE) == 2) {
                 // Tensor cores: D[p][jj] = sum_n S_c[n][p] v_jj[n] for the head's
                 // two row blocks (M = 128 value columns, K = N keys, A read from
@@ -1481,7 +1490,7 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
             for (int r0 = 0; r0 < hc; r0 += UPF) {
                 if (r0 > 0) {
 #pragma unroll
-                    for (int t = 0; t < UPF; ++t) upf[t] = r0 + t < hc ? ucol[slot(r0 + t) * ustride] : 0.f;
+                    for (int t = 0; t < UPF; ++t) upf[t] = r0 + t < hc ? u_at(r0 + t) : 0.f;
                 }
 #pragma unroll
                 for (int t = 0; t < UPF; ++t) {
@@ -1519,7 +1528,11 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
                         if (i3 <= i) yv = fmaf(cc2[i3], ud[i3], yv);
                     if (lead) {
                         unew[((size_t)j * TMAX + i) * P + pp] = u;
-                        if (append) static_cast<float *>(p.buf_v)[(((size_t)b * cap + slot(m)) * H + hh) * P + pp] = u;
+                        if (append) {
+                            const size_t ui = (((size_t)b * cap + slot(m)) * H + hh) * P + pp;
+                            if (u16) static_cast<uint16_t *>(p.buf_v)[ui] = (uint16_t)f2bf(u);
+                            else static_cast<float *>(p.buf_v)[ui] = u;
+                        }
                         p.y[(((size_t)b * T + i) * H + hh) * P + pp] = yv;
                     }
                 }

@@ -88,7 +88,7 @@ class Workload:
     capacity: int = 0    # circular buffer capacity (0 -> L)
     init_std: float = 0.0
     accept: str = ""     # "uniform" or "binomial0.7" for spec workloads
-    precision: str = "fp32"   # "fp32", "two", "shared_bf16"
+    precision: str = "fp32"   # "fp32", "two", "shared_bf16"; GDN "+u16": records keep u in bf16
 
     @property
     def cap(self) -> int:

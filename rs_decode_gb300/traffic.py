@@ -22,6 +22,7 @@ class Shape:
     G: int
     P: int
     N: int
+    u_bytes: int = 4                       # GDN records' u: 4 (fp32) or 2 (bf16)
 
     @property
     def state_elems(self) -> int:          # per sequence
@@ -31,8 +32,8 @@ class Shape:
     def record_bytes(self) -> int:         # one buffered record, per sequence
         if self.kind == "mamba2":          # x bf16, dt f32, alpha f32, B bf16
             return self.H * self.P * 2 + self.H * 4 + self.H * 4 + self.G * self.N * 2
-        # u f32, alpha f32 (one per head, or one per key channel with a per-channel decay), k bf16
-        return self.H * self.P * 4 + self.H * self.decays * 4 + self.G * self.N * 2
+        # u (fp32, or bf16), alpha f32 (one per head, or one per key channel with a per-channel decay), k bf16
+        return self.H * self.P * self.u_bytes + self.H * self.decays * 4 + self.G * self.N * 2
 
     @property
     def input_bytes(self) -> int:          # one step's inputs, per sequence

@@ -21,7 +21,7 @@ from rs_decode_gb300.layer import Layer, to_device
 TOL_HP = 2e-3
 TOL_LP = 3e-2
 
-PREC = {"fp32": rb.PREC_FP32, "two": rb.PREC_TWO, "shared_bf16": rb.PREC_SHARED_BF16}
+PREC = rb.PRECISIONS
 
 
 def rel_err(got, ref) -> np.ndarray:
