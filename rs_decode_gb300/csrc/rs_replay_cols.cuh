@@ -465,30 +465,43 @@ __device__ __forceinline__ void gather_fold_coefs(float *cfs, const FoldSrc &fs,
     __syncwarp();
 }
 
-// As gather_fold_coefs for fp32 records (GDN, KDA), without the factor fw_r
+// As gather_fold_coefs for GDN and KDA records, without the factor fw_r
 // (the caller applies it as it reads): the committed records' u go straight
 // from global memory to the scratch with cp.async, all of a lane's copies in
 // flight at once and no registers held; this launch's records (in shared
-// memory) are copied directly.
+// memory) are copied directly.  bf16 u (RS_U_BF16) lands in the upper half of
+// the item's 16-byte fp32 slot and is widened in place after the wait: each
+// lane widens only the items it copied.
 template <class C>
 __device__ __forceinline__ void gather_fold_values_async(float *cfs, const FoldSrc &fs, int nr, int wcol0,
                                                          int lane) {
-    static_assert(C::KIND != RS_MAMBA2, "fp32 record values");
+    static_assert(C::KIND != RS_MAMBA2, "GDN and KDA record values");
     constexpr int WC = C::P / C::NCW, Q = WC / 4;
     __syncwarp();  // the previous coefficients have been read
+    const int esz = fs.u16 ? 2 : 4;
     for (int i = lane; i < nr * Q; i += 32) {
         const int r = i / Q, c4 = i % Q;
         float *dst = cfs + r * WC + 4 * c4;
         if (r < fs.hc) {
             int sl = fs.base + r;
             if (sl >= fs.cap) sl -= fs.cap;
-            cp_async16(dst, fs.committed + (size_t)sl * fs.slot_stride + (size_t)(wcol0 + 4 * c4) * 4);
+            const uint8_t *src = fs.committed + (size_t)sl * fs.slot_stride + (size_t)(wcol0 + 4 * c4) * esz;
+            if (fs.u16) cp_async8(dst + 2, src);
+            else cp_async16(dst, src);
         } else {
             *reinterpret_cast<float4 *>(dst) = *reinterpret_cast<const float4 *>(
                 fs.fresh + (size_t)(r - fs.hc) * fs.fresh_stride + (size_t)(wcol0 + 4 * c4) * 4);
         }
     }
     cp_async_wait_all();
+    if (fs.u16) {
+        for (int i = lane; i < min(nr, fs.hc) * Q; i += 32) {
+            float *dst = cfs + (i / Q) * WC + 4 * (i % Q);
+            float v[4];
+            load_bf16_vec<4>(reinterpret_cast<const uint16_t *>(dst + 2), v);
+            *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+        }
+    }
     __syncwarp();
 }
 
@@ -597,8 +610,7 @@ __device__ __forceinline__ void fold_head(const ReplayParams &p, uint8_t *stages
             // lanes of a shared-memory phase still read one whole line; the
             // line's swizzle phase alternates with the row (NCB lines per row).
             const int cg = lane & 7, rg = lane >> 3, cb = wcol0 / W::CBE;
-            if (fs.u16) gather_fold_coefs<C>(cfs, fs, nullptr, 0, F > 0 ? F : 0, j, wcol0, lane);
-            else gather_fold_values_async<C>(cfs, fs, F > 0 ? F : 0, wcol0, lane);
+            gather_fold_values_async<C>(cfs, fs, F > 0 ? F : 0, wcol0, lane);
             for (int rb = 0; rb < NCB; ++rb) {
                 const uint8_t *sb = stages + (size_t)ring_add(q0, rb, NS).s * C::STAGE;
                 float o[8][4];
@@ -1404,13 +1416,19 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
             const int pl = (TC && C::UMMA && sizeof(TE) == 2) ? 32 * warp + lane : col0 + (rg >> (LR - ilog2(VEC)));
             const size_t uoff = ((size_t)b * cap * H + hh) * P + pl, ustride = (size_t)H * P;
             const bool u16 = p.u16 != 0;
-            auto u_at = [&](int r) {  // committed record r's u at the lane's column
-                const size_t i = uoff + slot(r) * ustride;
-                return u16 ? bf2f(static_cast<const uint16_t *>(p.buf_v)[i]) : static_cast<const float *>(p.buf_v)[i];
+            // A record's u is loaded as the aligned 32-bit word that holds it
+            // (bf16: the lane's half of two columns) and widened only where it
+            // is used, so that no instruction waits on the load before the dots.
+            const int esz = u16 ? 2 : 4;
+            const unsigned ush = u16 && !(pl & 1) ? 16u : 0u, umask = u16 ? 0xffff0000u : 0xffffffffu;
+            auto u_at = [&](int r) {  // committed record r's u at the lane's column, raw
+                const size_t i = (uoff + slot(r) * ustride) * esz;
+                return *reinterpret_cast<const unsigned *>(static_cast<const uint8_t *>(p.buf_v) + (i & ~(size_t)3));
             };
-            float upf[UPF];
+            auto u_val = [&](unsigned raw) { return __uint_as_float((raw << ush) & umask); };
+            unsigned upf[UPF];
 #pragma unroll
-            for (int t = 0; t < UPF; ++t) upf[t] = t < hc ? u_at(t) : 0.f;
+            for (int t = 0; t < UPF; ++t) upf[t] = t < hc ? u_at(t) : 0u;
             if constexpr (TC && C::UMMA && sizeof(TE) == 2) {
                 // Tensor cores: D[p][jj] = sum_n S_c[n][p] v_jj[n] for the head's
                 // two row blocks (M = 128 value columns, K = N keys, A read from
@@ -1490,17 +1508,18 @@ __device__ __forceinline__ bool consume_heads(const ReplayParams &p, uint8_t *sm
             for (int r0 = 0; r0 < hc; r0 += UPF) {
                 if (r0 > 0) {
 #pragma unroll
-                    for (int t = 0; t < UPF; ++t) upf[t] = r0 + t < hc ? u_at(r0 + t) : 0.f;
+                    for (int t = 0; t < UPF; ++t) upf[t] = r0 + t < hc ? u_at(r0 + t) : 0u;
                 }
 #pragma unroll
                 for (int t = 0; t < UPF; ++t) {
                     const int r = r0 + t;
                     if (r < hc) {
+                        const float uv = u_val(upf[t]);
 #pragma unroll
                         for (int i = 0; i < TMAX; ++i) {
                             if (i < T) {
-                                rs1[i] = fmaf(c1[(j * TMAX + i) * cap + r], upf[t], rs1[i]);
-                                rs2[i] = fmaf(c2[(j * TMAX + i) * cap + r], upf[t], rs2[i]);
+                                rs1[i] = fmaf(c1[(j * TMAX + i) * cap + r], uv, rs1[i]);
+                                rs2[i] = fmaf(c2[(j * TMAX + i) * cap + r], uv, rs2[i]);
                             }
                         }
                     }
