@@ -335,37 +335,53 @@ def measure_decode(w, K, W, dev, rank, world, want_eager=True, want_e2e=True, wa
     clocks = ClockSampler(dev.index or 0) if want_clocks else None
     if clocks:
         clocks.start()
-    ev = list(zip(_events(K), _events(K)))
     start, end = _events(2)
     barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
     start.record(stream)
     for s in range(K):
-        ev[s][0].record(stream)
         layer.decode(dev_steps[(W + s) % npool], gp, y)
-        ev[s][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     barrier()
     rows = clocks.stop() if clocks else None
     ms_total = start.elapsed_time(end)
+
+    # The folding / streaming split: K more launches after the timed region,
+    # each between its own pair of events (recording them costs host time,
+    # which would slow a host-bound small-batch loop if taken inside it).
+    hs = int(layer.h[0].item())
+    ev = list(zip(_events(K), _events(K)))
+    for s in range(K):
+        ev[s][0].record(stream)
+        layer.decode(dev_steps[(W + K + s) % npool], gp, y)
+        ev[s][1].record(stream)
+    torch.cuda.synchronize()
     launch_ms = [a.elapsed_time(b) for a, b in ev]
     if layer.status() != 0:
         raise RuntimeError("device status bits set during the benchmark")
 
-    # algorithmic bytes of the timed launches (the pointer schedule is lockstep)
+    # algorithmic bytes of the launches (the pointer schedule is lockstep)
     shape = traffic.Shape(w.kind, w.B, w.H, w.G, w.P, w.N, u_bytes=2 if "u16" in w.precision else 4)
-    total_bytes, h = 0, h0
     two = w.precision.startswith("two")
-    per_launch = []  # (folds, bytes, ms) of every timed launch
-    for s in range(K):
+
+    def launch_bytes(h):
         flush = h + 1 >= w.L
         rd = 4 if (flush or not two) else 2          # two-precision: bf16 copy off the flush steps
         wr = 6 if two else 4                          # a fold writes both copies
-        nb = traffic.replay_step_bytes(shape, h, flush, rd, wr)
+        return flush, traffic.replay_step_bytes(shape, h, flush, rd, wr)
+
+    total_bytes, folds_timed, h = 0, 0, h0
+    for s in range(K):  # the timed launches
+        flush, nb = launch_bytes(h)
         total_bytes += nb
+        folds_timed += flush
+        h = 0 if flush else h + 1
+    per_launch, h = [], hs  # (folds, bytes, ms) of every launch of the split pass
+    for s in range(K):
+        flush, nb = launch_bytes(h)
         per_launch.append((flush, nb, launch_ms[s]))
         h = 0 if flush else h + 1
 
@@ -386,7 +402,7 @@ def measure_decode(w, K, W, dev, rank, world, want_eager=True, want_e2e=True, wa
               "how": f"(1 folding + {w.L - 1} streaming launches) / {w.L}, from the per-launch events"}
     out = {"ms_total": ms_total, "ms_per_step": ms_total / K, "launch_ms": statistics.fmean(launch_ms),
            "bytes_per_launch": total_bytes / K, "clock_rows": rows, "t_wall": (t_wall0, t_wall1),
-           "fold_launch": fl, "stream_launch": sl, "window_weighted": ww, "folds_timed": sum(f for f, _, _ in per_launch),
+           "fold_launch": fl, "stream_launch": sl, "window_weighted": ww, "folds_timed": folds_timed,
            "eager": None, "e2e": None}
 
     if want_eager:
@@ -572,6 +588,65 @@ def measure_spec(w, rounds, W, dev, rank):
 
 
 # ----------------------------------------------------------------------------- sweeps
+def measure_decode_graph(w, dev, reps: int = 50) -> dict:
+    """GPU time per standard decode step of workload w, replay and eager alike:
+    two windows of steps (2L launches, each with its own inputs) captured in
+    one CUDA graph and replayed, so that the host's per-call cost, which bounds
+    a small batch launched step by step, drops out of both arms."""
+    import torch
+
+    from rs_decode_gb300 import binding as rb
+    from rs_decode_gb300 import synth, traffic
+    from rs_decode_gb300.layer import Layer, to_device
+
+    params, gp = _params(w, dev)
+    steps = [to_device(synth.step_inputs(w, s, seed=0, params=params), dev) for s in range(2 * w.L)]
+    layer = Layer(w.kind, w.B, w.H, w.G, w.P, w.N, w.L, capacity=w.cap, precision=rb.PRECISIONS[w.precision])
+    S0 = _init_state(layer, w, dev, 0)
+    S_e = S0.clone()
+    y = torch.empty(w.B, w.H, w.P, device=dev)
+
+    def replay():
+        for d in steps:
+            layer.decode(d, gp, y)
+
+    def eager():
+        for d in steps:
+            if w.kind == "mamba2":
+                rb.rs_eager_step_mamba2(layer.desc, S_e, d["x"], d["dt"], gp["A"], d["Bm"], d["Cm"], gp["D"], y)
+            else:
+                fn = rb.rs_eager_step_gdn if w.kind == "gdn" else rb.rs_eager_step_kda
+                fn(layer.desc, S_e, d["q"], d["k"], d["v"], d["alpha"], d["beta"], y)
+
+    def per_step_ms(fn):
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):  # warm-up (one-time set-up happens outside the capture)
+            fn()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            fn()
+        for _ in range(3):
+            g.replay()
+        a, b = _events(2)
+        torch.cuda.synchronize(dev)
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / (reps * len(steps))
+
+    ms_r, ms_e = per_step_ms(replay), per_step_ms(eager)
+    if layer.status() != 0:
+        raise RuntimeError("device status bits set during the benchmark")
+    shape = traffic.Shape(w.kind, w.B, w.H, w.G, w.P, w.N)
+    nb = sum(traffic.replay_step_bytes(shape, h, h + 1 >= w.L) for h in range(w.L)) / w.L
+    return {"ms_per_step": ms_r, "eager_ms_per_step": ms_e, "bytes_per_step": nb, "speedup_vs_eager": ms_e / ms_r}
+
+
 def run_sweeps(dev):
     """Window size L, batch B, draft count T and two-precision sweeps of the
     Mamba-2 serving layer (the pages' window trade-off and small-batch remark,
@@ -591,6 +666,13 @@ def run_sweeps(dev):
         print(json.dumps({"sweep": "window", "L": L, "B": 256, **dec(base.with_(L=L), K=16 * L)}), flush=True)
     for B in (1, 8, 32, 128, 512):
         print(json.dumps({"sweep": "batch", "L": 16, "B": B, **dec(base.with_(B=B))}), flush=True)
+    for B in (1, 4, 8, 16, 32):  # small batches, GPU time (CUDA-graph replay, both arms)
+        m = measure_decode_graph(base.with_(B=B), dev)
+        gbs = m["bytes_per_step"] / (m["ms_per_step"] * 1e-3) / 1e9
+        print(json.dumps({"sweep": "batch (graph replay)", "L": 16, "B": B,
+                          "tokens_per_s": B / (m["ms_per_step"] * 1e-3), "achieved_gbs": gbs, "frac": gbs / peak,
+                          "eager_tokens_per_s": B / (m["eager_ms_per_step"] * 1e-3),
+                          "speedup_vs_eager": m["speedup_vs_eager"]}), flush=True)
     print(json.dumps({"sweep": "precision", "precision": "two", "B": 256, "L": 16,
                       **dec(base.with_(precision="two"))}), flush=True)
     gdn = synth.WORKLOADS["gdn"]
@@ -686,7 +768,8 @@ def run_librs(args, rank: int, world: int, local_rank: int) -> dict | None:
                      "duration": "timed region / K (CUDA events on the launching stream)",
                      # the launches that fold the window (checkpoint read + write, the flush route) and
                      # the others (checkpoint read only), each against the same peak
-                     "fold_launch": frac_of(m["fold_launch"], peak), "stream_launch": frac_of(m["stream_launch"], peak)},
+                     "fold_launch": frac_of(m["fold_launch"], peak), "stream_launch": frac_of(m["stream_launch"], peak),
+                     "split": "K more launches after the timed region, each between its own events"},
         "hbm_gbs": achieved,
         "timed_region": {"starts_at_window_position": 0, "folds": m["folds_timed"], "window_L": w.L,
                          "whole_windows": K % w.L == 0},

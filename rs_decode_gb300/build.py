@@ -15,7 +15,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "librs.so")
-SOURCES = ["rs_api.cu", "rs_replay.cu", "rs_replay_m2.cu", "rs_replay_gdn.cu", "rs_replay_kda.cu", "rs_eager.cu",
+SOURCES = ["rs_api.cu", "rs_replay.cu", "rs_replay_m2.cu", "rs_replay_gdn.cu", "rs_replay_kda.cu", "rs_replay_direct.cu", "rs_eager.cu",
            "rs_small.cu", "rs_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

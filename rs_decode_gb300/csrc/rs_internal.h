@@ -93,6 +93,10 @@ cudaError_t replay_launch_m2_64x128(const ReplayParams &p, cudaStream_t s);
 cudaError_t replay_launch_gdn_128x128(const ReplayParams &p, cudaStream_t s);
 cudaError_t replay_launch_kda_128x128(const ReplayParams &p, cudaStream_t s);
 cudaError_t replay_launch_64x64(const ReplayParams &p, int kind, cudaStream_t s);
+// Small-batch Mamba-2 decode with the fp32 checkpoint: one CTA per two heads,
+// no pipeline (rs_replay_direct.cu).
+bool replay_direct_applies(const ReplayParams &p, int kind, int P, int N);
+cudaError_t replay_direct_launch(const ReplayParams &p, cudaStream_t s);
 cudaError_t eager_launch(const EagerParams &p, int kind, int P, int N, cudaStream_t s);
 
 // Small kernels (rs_small.cu).

@@ -107,6 +107,7 @@ cudaError_t replay_launch_64x64(const ReplayParams &p, int kind, cudaStream_t s)
 }
 
 cudaError_t replay_launch(const ReplayParams &p, int kind, int P, int N, cudaStream_t s) {
+    if (replay_direct_applies(p, kind, P, N)) return replay_direct_launch(p, s);
     if (kind == RS_MAMBA2 && P == 64 && N == 128) return replay_launch_m2_64x128(p, s);
     if (kind == RS_GDN && P == 128 && N == 128) return replay_launch_gdn_128x128(p, s);
     if (kind == RS_KDA && P == 128 && N == 128) return replay_launch_kda_128x128(p, s);

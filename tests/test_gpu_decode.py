@@ -172,3 +172,54 @@ def test_gdn_forced_flush_and_materialize():
             assert (run.layer.pointers()["h"] == 0).all()
             assert rel_err(run.checkpoint(), run.model.S).max() <= TOL_HP
     assert rel_err(run.materialized(), run.model.S).max() <= TOL_HP
+
+
+def test_small_batch_kernel_and_pipeline_share_the_state():
+    """At B = 8, standard steps of the fp32 Mamba-2 layer run on the
+    small-batch kernel and verify rounds on the streaming pipeline, so each
+    reads records, pointers and checkpoints that the other wrote: standard
+    steps, rounds of 4 drafts with commits, and standard steps again across
+    folds, all against the oracle."""
+    import oracle
+    from harness import gpu_params, state_np_to_gpu
+    from oracle.pointers import Pointers
+    from rs_decode_gb300.layer import to_device
+
+    w = synth.WORKLOADS["mamba2_spec"].with_(B=8)
+    seed = 9
+    params = synth.layer_params(w, seed)
+    gp = gpu_params(w, params)
+    S0 = synth.initial_state(w, seed)
+    layer = make_layer(w)
+    layer.init(state_np_to_gpu(S0))
+    model = oracle.Model(w.kind, S0, params)
+    ptrs = [Pointers(w.L, w.cap) for _ in range(w.B)]
+    heads = HeadErr(w.H)
+    t = r = folds = 0
+    for phase, n in (("std", 11), ("spec", 5), ("std", 13), ("spec", 6), ("std", 17)):
+        for _ in range(n):
+            if phase == "std":
+                d = synth.step_inputs(w, t, seed, params)
+                y = layer.decode(to_device(d), gp).cpu().numpy()
+                y_ref = model.step(d)
+                folds += sum(p.standard_step() > 0 for p in ptrs)
+                t += 1
+            else:
+                d = synth.round_inputs(w, r, seed, params)
+                dev = to_device(d)
+                y = layer.verify(w.T, dev, gp).cpu().numpy()
+                folds += sum(p.verify(w.T) > 0 for p in ptrs)
+                y_ref = model.spec_round(d)
+                layer.commit(dev["accepted"])
+                for p, a in zip(ptrs, d["accepted"]):
+                    p.commit(int(a))
+                r += 1
+            e = rel_err(y, y_ref).max()
+            assert e <= TOL_HP, f"{phase} call {t + r}: output rel err {e:.3e}"
+            heads.add(y, y_ref)
+            ptr = layer.pointers()
+            assert (ptr["h"] == [p.h for p in ptrs]).all() and (ptr["base"] == [p.base for p in ptrs]).all()
+    assert folds >= 2 * w.B
+    assert heads.worst() <= TOL_HP
+    assert rel_err(state_gpu_to_np(layer.materialize()), model.S).max() <= TOL_HP
+    assert layer.status() == 0
