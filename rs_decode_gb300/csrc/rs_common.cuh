@@ -32,6 +32,28 @@ __device__ __forceinline__ void st_stream(void *p, uint4 v) { __stcs(reinterpret
 __device__ __forceinline__ void st_stream2(void *p, uint2 v) { __stcs(reinterpret_cast<uint2 *>(p), v); }
 __device__ __forceinline__ uint4 ld_u4(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
 
+// Paired fp32 arithmetic (fma.rn.f32x2, mul.rn.f32x2; sm_100 and later): one
+// instruction computes two lanes held in a 64-bit register pair, with the
+// rounding of two separate fp32 operations.
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+    return (unsigned long long)__float_as_uint(hi) << 32 | __float_as_uint(lo);
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long v, float &lo, float &hi) {
+    lo = __uint_as_float((unsigned)v);
+    hi = __uint_as_float((unsigned)(v >> 32));
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // Asynchronous global -> shared copies (cp.async): a CTA issues all of its
 // small staging loads back to back and waits once.
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {

@@ -53,6 +53,10 @@ struct PipeCfg {
     // registers sized so that two CTAs fit on an SM (two-stage rings; the
     // draft-heavy T=8 shape excepted)
     static constexpr int MIN_BLOCKS = (NS <= 2 && TMAX <= 4) ? 2 : 1;
+    // a folding unit converts its records' keys to fp32 once (single-query
+    // launches: standard decode, flush, materialise); the draft buckets, whose
+    // shared memory is fuller, convert key pairs as the fold reads them
+    static constexpr bool KF = TMAX == 1;
 };
 
 // A unit's plan as the producer hands it to the consumers (b = -1: no more units).
@@ -63,7 +67,7 @@ struct RowPlan {
 
 // Shared-memory carve-up, byte offsets (16-byte aligned; stages first).
 struct PipeSmem {
-    int stages, bars, plans, abort, kraw, xr, ar, sr, cst, vb, bt, d1, d2, c1, c2, g1, g2, fw, gF, pre1, pre2, red,
+    int stages, bars, plans, abort, kraw, xr, ar, sr, cst, vb, bt, d1, d2, c1, c2, g1, g2, fw, gF, pre1, pre2, red, kf,
         total;
 };
 
@@ -79,6 +83,7 @@ __host__ __device__ inline PipeSmem pipe_smem(int cap) {
     s.bars = o;   o += al16((2 * C::NS + 4) * 8);
     s.plans = o;  o += al16(2 * (int)sizeof(RowPlan));
     s.abort = o;  o += 16;
+    s.kf = o;     o += C::KF ? cap * N * 4 : 0;                     // folded records' keys, fp32 (just below kraw)
     s.kraw = o;   o += al16((cap + TMAX) * N * 2);                  // bf16 keys (rows < cap), queries (cap + i)
     s.xr = o;     o += al16(HU * cap * P * (GDN ? 4 : 2));          // Mamba-2 x bf16 / GDN u fp32 per record
     s.ar = o;     o += al16(HU * cap * 4);                          // decays alpha_r
@@ -197,21 +202,31 @@ __device__ __forceinline__ void producer(const ReplayParams &p, uint8_t *sm, con
 // ---------------------------------------------------------------------------
 // Fold of one staged row block: S_new = gF S_c + sum_{r<F} (fw_r v_r) k_r^T,
 // written to the checkpoint (both copies as present) or to the materialise
-// output.  The coefficient fw_r v_r of this thread's columns is formed once per
-// record and applied to all R rows the thread owns.  The warp hands the stage
+// output.  The thread's R rows are held as R/2 row pairs per column, so that
+// one paired FMA (fma.rn.f32x2) applies a record to two rows: the record's
+// keys for the rows are pairs as loaded (fp32 keys kf, or bf16 pairs widened
+// with two integer operations), and the coefficient fw_r v_r of a column is
+// formed once per record and broadcast into a pair.  The warp hands the stage
 // back (one arrival on `empty`) as soon as its rows are in registers, so the
 // next copy overlaps the fold's arithmetic and stores.
 template <class C, typename TE, int R, int VEC>
 __device__ __forceinline__ void fold_block(const ReplayParams &p, const TE *blk, uint64_t *empty, const uint16_t *kraw,
-                                           const uint16_t *xb, const float *uf, const float *fw, float gf, int F,
-                                           int cap, int j, int row0, int n0p, int p0, size_t goff, bool materialize) {
-    constexpr int P = C::P, N = C::N;
-    float o[R][VEC];
+                                           const uint16_t *xb, const float *uf, const float *fw,
+                                           float gf, int F, int cap, int j, int row0, int n0p, int p0, size_t goff,
+                                           bool materialize) {
+    constexpr int P = C::P, N = C::N, RP = R / 2;
+    static_assert(R % 2 == 0, "rows are folded in pairs");
+    unsigned long long o2[RP][VEC];
+    {
+        const unsigned long long g2 = f2_pack(gf, gf);
 #pragma unroll
-    for (int k = 0; k < R; ++k) {
-        unpack<TE, VEC>(ld_u4(blk + (size_t)(n0p + k) * P + p0), o[k]);
+        for (int i = 0; i < RP; ++i) {
+            float a[VEC], b[VEC];
+            unpack<TE, VEC>(ld_u4(blk + (size_t)(n0p + 2 * i) * P + p0), a);
+            unpack<TE, VEC>(ld_u4(blk + (size_t)(n0p + 2 * i + 1) * P + p0), b);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) o[k][e] *= gf;
+            for (int e = 0; e < VEC; ++e) o2[i][e] = f2_mul(f2_pack(a[e], b[e]), g2);
+        }
     }
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(empty);
@@ -230,21 +245,43 @@ __device__ __forceinline__ void fold_block(const ReplayParams &p, const TE *blk,
                 cf[e] = w * u4.x; cf[e + 1] = w * u4.y; cf[e + 2] = w * u4.z; cf[e + 3] = w * u4.w;
             }
         }
-        float kr[R];
-        load_bf16_run<R>(kraw + (size_t)r * N + row0 + n0p, kr);
+        unsigned long long kp[RP];
+        if constexpr (C::KF) {  // the fp32 keys lie just below the bf16 ones
+            // a pair of consecutive fp32 keys is one 64-bit word, the lower row low
+            const unsigned long long *kr = reinterpret_cast<const unsigned long long *>(
+                reinterpret_cast<const float *>(kraw) - (size_t)(cap - r) * N + row0 + n0p);
 #pragma unroll
-        for (int k = 0; k < R; ++k)
+            for (int i = 0; i < RP; ++i) kp[i] = kr[i];
+        } else {
+            const uint32_t *kw = reinterpret_cast<const uint32_t *>(kraw + (size_t)r * N + row0 + n0p);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) o[k][e] = fmaf(cf[e], kr[k], o[k][e]);
+            for (int i = 0; i < RP; ++i) {
+                const uint32_t u = kw[i];
+                kp[i] = f2_pack(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            const unsigned long long cb = f2_pack(cf[e], cf[e]);
+#pragma unroll
+            for (int i = 0; i < RP; ++i) o2[i][e] = f2_fma(kp[i], cb, o2[i][e]);
+        }
     }
 #pragma unroll
-    for (int k = 0; k < R; ++k) {
-        const size_t off = goff + (size_t)(row0 + n0p + k) * P + p0;
-        if (materialize) {
-            store_f32<VEC>(p.out + off, o[k]);
-        } else {
-            if (p.ckpt_hp) store_f32<VEC>(p.ckpt_hp + off, o[k]);
-            if (p.ckpt_lp) store_bf16<VEC>(p.ckpt_lp + off, o[k]);
+    for (int i = 0; i < RP; ++i) {
+        float a[VEC], b[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) f2_unpack(o2[i][e], a[e], b[e]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float(&o)[VEC] = h ? b : a;
+            const size_t off = goff + (size_t)(row0 + n0p + 2 * i + h) * P + p0;
+            if (materialize) {
+                store_f32<VEC>(p.out + off, o);
+            } else {
+                if (p.ckpt_hp) store_f32<VEC>(p.ckpt_hp + off, o);
+                if (p.ckpt_lp) store_bf16<VEC>(p.ckpt_lp + off, o);
+            }
         }
     }
 }
@@ -350,7 +387,21 @@ __device__ __forceinline__ bool consume_unit(const ReplayParams &p, uint8_t *sm,
     }
     if (named_sync_or(1, NC, false)) return false;
 
-    // ---- 2. new records' decays; appends
+    // ---- 2. the folded records' keys in fp32 (single-query configurations); new
+    // records' decays; appends
+    if constexpr (C::KF) {
+        if (keep) {
+            float *kf = reinterpret_cast<float *>(kraw) - (size_t)cap * N;
+            for (int i2 = tid; i2 < F * (N / 8); i2 += NC) {
+                const int r = i2 / (N / 8), c = i2 % (N / 8);
+                float f[8];
+                unpack<uint16_t, 8>(ld_u4(kraw + (size_t)r * N + 8 * c), f);
+                float4 *d = reinterpret_cast<float4 *>(kf + (size_t)r * N + 8 * c);
+                d[0] = make_float4(f[0], f[1], f[2], f[3]);
+                d[1] = make_float4(f[4], f[5], f[6], f[7]);
+            }
+        }
+    }
     for (int i2 = tid; i2 < HU * T; i2 += NC) {
         const int i = i2 / HU, hd = i2 % HU, hh = h0 + hd, r = hc + i;
         float a;
