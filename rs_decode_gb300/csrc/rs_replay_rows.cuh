@@ -68,7 +68,7 @@ struct RowPlan {
 // Shared-memory carve-up, byte offsets (16-byte aligned; stages first).
 struct PipeSmem {
     int stages, bars, plans, abort, kraw, xr, ar, sr, cst, vb, bt, d1, d2, c1, c2, g1, g2, fw, gF, pre1, pre2, red, kf,
-        total;
+        qf, total;
 };
 
 __host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
@@ -102,6 +102,7 @@ __host__ __device__ inline PipeSmem pipe_smem(int cap) {
     s.pre1 = o;   o += al16(HU * TMAX * P * 4);                     // record parts of the outputs
     s.pre2 = o;   o += GDN ? al16(HU * TMAX * P * 4) : 0;
     s.red = o;    o += al16(2 * C::NCW * C::JMAX * P * 4);          // double-buffered warp partials
+    s.qf = o;     o += C::JMAX > 2 ? al16(N * C::JMAX * 4) : 0;     // draft buckets: dot vectors, fp32 [N][JMAX]
     s.total = o;
     return s;
 }
@@ -387,8 +388,17 @@ __device__ __forceinline__ bool consume_unit(const ReplayParams &p, uint8_t *sm,
     }
     if (named_sync_or(1, NC, false)) return false;
 
-    // ---- 2. the folded records' keys in fp32 (single-query configurations); new
-    // records' decays; appends
+    // ---- 2. the folded records' keys in fp32 (single-query configurations); the
+    // dot vectors in fp32, key-major (draft buckets); new records' decays; appends
+    if constexpr (JMAX > 2) {
+        float *qf = reinterpret_cast<float *>(sm + L.qf);
+        for (int i2 = tid; i2 < N * JMAX; i2 += NC) {
+            const int jj = i2 % JMAX, n = i2 / JMAX;
+            // Mamba-2: q_jj ; GDN: jj < T -> k_{hc+jj}, else q_{jj-T}
+            const int row = (KIND == RS_GDN && jj < T) ? hc + jj : cap + (KIND == RS_GDN ? jj - T : jj);
+            qf[i2] = jj < J ? bf2f(kraw[(size_t)row * N + n]) : 0.f;
+        }
+    }
     if constexpr (C::KF) {
         if (keep) {
             float *kf = reinterpret_cast<float *>(kraw) - (size_t)cap * N;
@@ -578,6 +588,11 @@ __device__ __forceinline__ bool consume_unit(const ReplayParams &p, uint8_t *sm,
         for (int a = 0; a < JMAX; ++a)
 #pragma unroll
             for (int e = 0; e < VEC; ++e) acc[a][e] = 0.f;
+        unsigned long long acc2[JMAX > 2 ? JMAX / 2 : 1][VEC];  // draft buckets: vector pairs per column
+#pragma unroll
+        for (int m = 0; m < (JMAX > 2 ? JMAX / 2 : 1); ++m)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) acc2[m][e] = 0ull;
         bool ok = true;
         for (int part = 0; part < SPLIT; ++part, ++it) {
             const int st = it % NS;
@@ -625,22 +640,25 @@ __device__ __forceinline__ bool consume_unit(const ReplayParams &p, uint8_t *sm,
                         }
                     }
                 } else {
-                    // more vectors: their values are read per row (fewer live
-                    // registers in the draft buckets)
+                    // more vectors (draft buckets): a row's vector values are
+                    // one fp32 run of qf, consecutive vectors pairing up, and
+                    // each slab value is broadcast into a pair, so that one
+                    // paired FMA serves two vectors
+                    const float *qf = reinterpret_cast<const float *>(sm + L.qf);
 #pragma unroll
                     for (int k = 0; k < R; ++k) {
                         float sv[VEC];
                         unpack<TE, VEC>(ld_u4(blk + (size_t)(n0p + k) * P + p0), sv);
+                        const unsigned long long *wq =
+                            reinterpret_cast<const unsigned long long *>(qf + (size_t)(row0 + k) * JMAX);
+                        unsigned long long w2[JMAX / 2];
 #pragma unroll
-                        for (int jj = 0; jj < JMAX; ++jj) {
-                            if (jj < J) {
-                                // Mamba-2: q_jj ; GDN: jj < T -> k_{hc+jj}, else q_{jj-T}
-                                const int row =
-                                    (KIND == RS_GDN && jj < T) ? hc + jj : cap + (KIND == RS_GDN ? jj - T : jj);
-                                const float w = bf2f(kraw[(size_t)row * N + row0 + k]);
+                        for (int m = 0; m < JMAX / 2; ++m) w2[m] = wq[m];
 #pragma unroll
-                                for (int e = 0; e < VEC; ++e) acc[jj][e] = fmaf(sv[e], w, acc[jj][e]);
-                            }
+                        for (int e = 0; e < VEC; ++e) {
+                            const unsigned long long sb = f2_pack(sv[e], sv[e]);
+#pragma unroll
+                            for (int m = 0; m < JMAX / 2; ++m) acc2[m][e] = f2_fma(w2[m], sb, acc2[m][e]);
                         }
                     }
                 }
@@ -649,6 +667,12 @@ __device__ __forceinline__ bool consume_unit(const ReplayParams &p, uint8_t *sm,
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty + st);
             }
+        }
+        if constexpr (JMAX > 2) {
+#pragma unroll
+            for (int m = 0; m < JMAX / 2; ++m)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) f2_unpack(acc2[m][e], acc[2 * m][e], acc[2 * m + 1][e]);
         }
         // intra-warp reduction over the row groups of the warp, then per-warp partials
 #pragma unroll
