@@ -847,6 +847,14 @@ cudaError_t launch_shape(const ReplayParams &p, cudaStream_t s) {
     cudaError_t e = cudaErrorInvalidValue;
     constexpr int DEEP = 4;
     if ((try_shape<PipeCfg<KIND, P, N, HUS, TMAX, NC, 2, SPLIT>>(p, hpg, kTwoPerSm, s, e) || ...)) return e;
+    if constexpr (TMAX == 8) {
+        // the 8-draft bucket prefers more heads per unit with three stages to
+        // fewer with four (B = 256, 8 drafts: 8 heads and 3 stages 0.616 ms per
+        // round, 4 heads and 4 stages 0.837 ms)
+        if (((try_shape<PipeCfg<KIND, P, N, HUS, TMAX, NC, DEEP, SPLIT>>(p, hpg, kMaxSmemPerBlock, s, e) ||
+              try_shape<PipeCfg<KIND, P, N, HUS, TMAX, NC, 3, SPLIT>>(p, hpg, kMaxSmemPerBlock, s, e)) || ...))
+            return e;
+    }
     if ((try_shape<PipeCfg<KIND, P, N, HUS, TMAX, NC, DEEP, SPLIT>>(p, hpg, kMaxSmemPerBlock, s, e) || ...)) return e;
     if ((try_shape<PipeCfg<KIND, P, N, HUS, TMAX, NC, 2, SPLIT>>(p, hpg, kMaxSmemPerBlock, s, e) || ...)) return e;
     return cudaErrorInvalidConfiguration;

@@ -33,6 +33,7 @@ import os
 import numpy as np
 import pytest
 
+import bench
 from harness import TOL_HP, TOL_LP, HeadErr, SpecRun, StandardRun, parity_sample, rel_err, state_errs
 from rs_decode_gb300 import synth
 
@@ -159,7 +160,9 @@ def test_gdn_spec_two_precision_full_length():
     report = {"metric": "per (round, sequence) normwise relative output error vs the fp64 oracle, all T drafts",
               "test": "tests/test_gpu_configs.py::test_gdn_spec_two_precision_full_length",
               "two_precision": rep["two_precision"], "shared_bf16": rep["shared_bf16"],
-              "workload": rep["workload"], "sample": rep["sample"], "slow_decay_variant": rep_slow}
+              "workload": rep["workload"], "sample": rep["sample"], "slow_decay_variant": rep_slow,
+              # the GDN kernel sources this run measured (the benchmark reports the record only for them)
+              "source_hash": bench.kernel_source_hash("gdn")}
     print(json.dumps(report))
     out = os.environ.get("RS_REPORT_DIR")
     if out:
