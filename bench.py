@@ -683,7 +683,7 @@ def run_sweeps(dev):
                           "tokens_per_s": gdn.B / (m["ms_per_step"] * 1e-3), "bytes_per_step": m["bytes_per_launch"],
                           "achieved_gbs": gbs, "frac": gbs / peak}), flush=True)
     spec = synth.WORKLOADS["mamba2_spec"]
-    for T in (1, 2, 4, 8):
+    for T in (1, 2, 4, 5, 8):
         o = measure_spec(spec.with_(T=T, capacity=16 + T), 64, 8, dev, 0)
         print(json.dumps({"sweep": "drafts", "T": T, "B": 256, "L": 16,
                           "verified_tokens_per_s": o["verified_tokens_per_s"],
