@@ -51,8 +51,9 @@ struct PipeCfg {
     static constexpr int STAGE = NP * P * 4;              // bytes of one fp32 row block = one stage
     static_assert(NS >= SPLIT, "a folding head keeps all its row blocks resident");
     // registers sized so that two CTAs fit on an SM (two-stage rings; the
-    // draft-heavy T=8 shape excepted)
-    static constexpr int MIN_BLOCKS = (NS <= 2 && TMAX <= 4) ? 2 : 1;
+    // draft-heavy T=8 shape excepted), three for the four-warp shapes of up to
+    // 4 drafts (two for their 8-draft shape)
+    static constexpr int MIN_BLOCKS = NC == 128 ? (TMAX <= 4 ? 3 : 2) : (NS <= 2 && TMAX <= 4) ? 2 : 1;
     // a folding unit converts its records' keys to fp32 once (single-query
     // launches: standard decode, flush, materialise); the draft buckets, whose
     // shared memory is fuller, convert key pairs as the fold reads them
@@ -826,13 +827,15 @@ cudaError_t launch_pipe(const ReplayParams &p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-// Launch shapes, tried in order: two CTAs per SM with a two-stage ring (one
-// CTA's per-unit and per-head serial phases overlap the other's streaming);
-// else one CTA per SM with a deeper ring that covers those phases itself;
-// else one CTA with two stages.  Within a tier, the most heads per unit whose
-// count divides the group and whose shared memory fits.
+// Launch shapes, tried in order: (four-warp configurations of up to 4 drafts)
+// three CTAs per SM; two CTAs per SM with a two-stage ring (one CTA's per-unit
+// and per-head serial phases overlap the other's streaming); else one CTA per
+// SM with a deeper ring that covers those phases itself; else one CTA with two
+// stages.  Within a tier, the most heads per unit whose count divides the group
+// and whose shared memory fits.
 constexpr int kMaxSmemPerBlock = 227 * 1024;
 constexpr int kTwoPerSm = kMaxSmemPerBlock / 2 - 1024;
+constexpr int kThreePerSm = kMaxSmemPerBlock / 3 - 1024;
 
 template <class C>
 bool try_shape(const ReplayParams &p, int hpg, int limit, cudaStream_t s, cudaError_t &err) {
@@ -846,6 +849,8 @@ cudaError_t launch_shape(const ReplayParams &p, cudaStream_t s) {
     const int hpg = p.H / p.G;
     cudaError_t e = cudaErrorInvalidValue;
     constexpr int DEEP = 4;
+    if constexpr (NC == 128 && TMAX <= 4)
+        if ((try_shape<PipeCfg<KIND, P, N, HUS, TMAX, NC, 2, SPLIT>>(p, hpg, kThreePerSm, s, e) || ...)) return e;
     if ((try_shape<PipeCfg<KIND, P, N, HUS, TMAX, NC, 2, SPLIT>>(p, hpg, kTwoPerSm, s, e) || ...)) return e;
     if constexpr (TMAX == 8) {
         // the 8-draft bucket prefers more heads per unit with three stages to
