@@ -223,3 +223,35 @@ def test_small_batch_kernel_and_pipeline_share_the_state():
     assert heads.worst() <= TOL_HP
     assert rel_err(state_gpu_to_np(layer.materialize()), model.S).max() <= TOL_HP
     assert layer.status() == 0
+
+
+@pytest.mark.parametrize("precision", ["fp32", "two", "shared_bf16"])
+def test_mamba2_step_shape_at_b64(precision):
+    """B = 64 is the smallest batch whose standard steps take the four-warp,
+    three-stage row-split shape (half-slab stages): every checkpoint precision
+    across two folds, a forced flush between them and materialised states,
+    on sampled sequences against the oracle."""
+    w = synth.WORKLOADS["mamba2"].with_(B=64)
+    sample = [0, 17, 42, 63]
+    run = StandardRun(w, seed=12, precision=precision, sample=sample)
+    heads = HeadErr(w.H)
+    tol_y = TOL_HP if precision == "fp32" else TOL_LP
+    for s in range(37):
+        y, y_ref, folded = run.step()
+        tol = TOL_HP if (precision == "two" and folded) else tol_y
+        e = rel_err(y, y_ref).max()
+        assert e <= tol, f"step {s}: output rel err {e:.3e} > {tol}"
+        heads.add(y, y_ref)
+        if folded or s == 20:
+            if s == 20:
+                run.layer.flush()
+                run.ptr.flush()
+            ck = rel_err(run.checkpoint(), run.model.S).max()
+            assert ck <= (TOL_LP if precision == "shared_bf16" else TOL_HP), f"step {s}: checkpoint rel err {ck:.3e}"
+        if s % 9 == 4:
+            m = rel_err(run.materialized(), run.model.S).max()
+            assert m <= TOL_HP if precision != "shared_bf16" else m <= TOL_LP, f"step {s}: materialised rel err {m:.3e}"
+    assert heads.worst() <= tol_y
+    ptr = run.layer.pointers()
+    assert (ptr["h"][run.idx] == run.ptr.h).all() and (ptr["base"][run.idx] == run.ptr.base).all()
+    assert run.layer.status() == 0
