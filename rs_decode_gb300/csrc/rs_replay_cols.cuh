@@ -353,7 +353,7 @@ __device__ __forceinline__ void reduce_rows(float (&acc)[WGeo<C, TE>::M], int rg
 // b = -1 ends the pipeline.  Units are assigned round-robin (u0, u0 + ustride,
 // ...): handing them out from one counter, as the row-split pipeline does,
 // measured slower here (the two-precision GDN round 0.369 against 0.324 ms,
-// same box).
+// same GPU).
 template <class C>
 __device__ __forceinline__ void planner(const ReplayParams &p, uint8_t *sm, const RSmem &L, int units, int HU,
                                         int NS, const PipeCtx &pc) {

@@ -5,7 +5,7 @@
 // flush, materialise) does the same, three CTAs per SM with three stages and 4
 // heads per unit, where that shape fits the buffer capacity and the batch gives
 // every CTA several units; otherwise (small batches, long windows) it keeps 8
-// consumer warps, whole-slab stages and two CTAs per SM.  B = 256, same box,
+// consumer warps, whole-slab stages and two CTAs per SM.  B = 256, same GPU,
 // against the 8-warp shape: one step 0.1779 against 0.1806 ms, 4 drafts 0.257
 // against 0.287 ms per round, 8 drafts 0.567 against 0.615 ms; but one step at
 // B = 32 0.727 against 0.744 of the copy peak and at L = 32 0.738 against 0.849.
