@@ -1,4 +1,5 @@
-"""Model check of the stage-ring protocol of the column-split replay kernel.
+"""Model check of the stage-ring protocol of the replay kernels (the column
+split, and with per-head hold flags the row split).
 
 The kernel streams checkpoint row blocks through a ring of NS shared-memory
 stages.  Each stage has a "full" mbarrier (one producer arrival plus the
@@ -60,9 +61,12 @@ class MBarrier:
 
 
 def simulate(NS: int, heads: list[int], NCW: int, seed: int, own_blocks_only: bool = False,
-             max_events: int = 400_000):
+             max_events: int = 400_000, held: list[bool] | None = None):
     """heads: blocks per head in stream order (2 for a bf16 head, 4 for an
-    fp32 head).  Returns (errors, drained)."""
+    fp32 head).  held (the row split): per head, whether its blocks are held
+    until all are read (a folding head) or each is released right after its
+    read (a streamed head); None: every head is held (the column split).
+    Returns (errors, drained)."""
     rnd = random.Random(seed)
     if own_blocks_only:  # the first design: as many arrivals as warps per column block
         assert len(set(heads)) == 1 and NCW % heads[0] == 0
@@ -125,6 +129,8 @@ def simulate(NS: int, heads: list[int], NCW: int, seed: int, own_blocks_only: bo
                 errors.append(("stale read", actor, w.q, data[s]))
             if own_blocks_only:
                 empty[s].arrive()            # the first design: its one block, at once
+            elif held is not None and not held[positions[w.q][0]]:
+                empty[s].arrive()            # a streamed row-split head: each block after its read
             else:
                 w.held.append(w.q)           # the head's blocks are all waited on first
             w.q += 1
@@ -189,3 +195,25 @@ def test_tensor_core_heads_occupy_adjacent_stages():
             if nb == 2:
                 assert q % 2 == 0 and (q % NS) + 1 == (q + 1) % NS
             q += nb
+
+
+@pytest.mark.parametrize("NS,SPLIT,NCW", [(2, 1, 8), (2, 2, 4), (3, 2, 4), (4, 1, 8), (4, 2, 4), (3, 1, 8)])
+def test_row_split_rings(NS, SPLIT, NCW):
+    """The row split's shapes: SPLIT row blocks per head (1: whole slabs, 2:
+    half slabs), rings of NS >= SPLIT stages, 8 or 4 consumer warps; streamed
+    heads release each block after its read, folding heads (about one in six
+    here, at random) hold all of theirs until the fold has read them."""
+    for seed in range(30):
+        rnd = random.Random(1000 + seed)
+        n = 16
+        held = [rnd.random() < 0.17 for _ in range(n)]
+        errors, drained = simulate(NS, [SPLIT] * n, NCW=NCW, seed=seed, held=held)
+        assert not errors, errors[:3]
+        assert drained, f"NS={NS} SPLIT={SPLIT} seed={seed}: did not drain"
+
+
+def test_row_split_fold_needs_a_ring_as_deep_as_a_head():
+    """A folding head of two row blocks cannot be held in a one-stage ring
+    (the launch shapes never pick one); streamed heads alone drain."""
+    assert simulate(1, [2, 2, 2], NCW=4, seed=3, held=[False, True, False]) == ([], False)
+    assert simulate(1, [2, 2, 2], NCW=4, seed=3, held=[False, False, False]) == ([], True)
