@@ -148,3 +148,17 @@ def test_traffic_records_are_keyed_by_their_kernels_sources():
         assert "rs_replay_cols.cuh" in bench.KERNEL_SOURCES[wl]
         assert "rs_replay_rows.cuh" not in bench.KERNEL_SOURCES[wl]
     assert len({bench.kernel_source_hash(w) for w in ("mamba2", "gdn", "kda")}) == 3
+
+
+def test_algorithmic_bytes_with_bf16_u_records():
+    """GDN records that keep u in bf16: a record's u costs 2 bytes per value
+    instead of 4 (H_v x d_v = 32 x 128 values, 8 KiB instead of 16 KiB), and
+    nothing else changes: the gdn workload's count with the smaller record."""
+    from rs_decode_gb300 import traffic
+    g32 = traffic.Shape("gdn", 256, 32, 16, 128, 128)
+    g16 = traffic.Shape("gdn", 256, 32, 16, 128, 128, u_bytes=2)
+    assert g32.record_bytes - g16.record_bytes == 32 * 128 * 2
+    assert g32.input_bytes == g16.input_bytes and g32.state_elems == g16.state_elems
+    avg = sum(traffic.replay_step_bytes(g16, h, flush=(h == 15)) for h in range(16)) / 16
+    rec, inp, out, ck = 8 * 1024 + 128 + 4096, 16 * 1024 + 256, 16 * 1024, 2 * 2**20
+    assert avg == 256 * (ck + ck / 16 + 7.5 * rec + 15 / 16 * rec + inp + out) == 605698048
