@@ -853,8 +853,9 @@ cudaError_t launch_shape(const ReplayParams &p, cudaStream_t s) {
         if ((try_shape<PipeCfg<KIND, P, N, HUS, TMAX, NC, 2, SPLIT>>(p, hpg, kThreePerSm, s, e) || ...)) return e;
     if ((try_shape<PipeCfg<KIND, P, N, HUS, TMAX, NC, 2, SPLIT>>(p, hpg, kTwoPerSm, s, e) || ...)) return e;
     if constexpr (TMAX == 8) {
-        // the 8-draft bucket prefers more heads per unit with three stages to
-        // fewer with four (B = 256, 8 drafts: 8 heads and 3 stages 0.616 ms per
+        // one CTA per SM (buffers too large for two): the 8-draft bucket
+        // prefers more heads per unit with three stages to fewer with four (8
+        // consumer warps, B = 256, 8 drafts: 8 heads and 3 stages 0.616 ms per
         // round, 4 heads and 4 stages 0.837 ms)
         if (((try_shape<PipeCfg<KIND, P, N, HUS, TMAX, NC, DEEP, SPLIT>>(p, hpg, kMaxSmemPerBlock, s, e) ||
               try_shape<PipeCfg<KIND, P, N, HUS, TMAX, NC, 3, SPLIT>>(p, hpg, kMaxSmemPerBlock, s, e)) || ...))
