@@ -840,7 +840,14 @@ __device__ __forceinline__ bool kda_scan(const ReplayParams &p, uint8_t *cx, con
         // the records' decay vectors are loaded CA records at a time, ahead of
         // their use (they come from L2 or HBM; the scan is sequential)
         constexpr int CA = TMAX <= 3 ? 8 : 4;
+        // one query (standard steps): the chunk's per-lane partial dots are kept
+        // and reduced across the warp together after the chunk, one 16-value
+        // reduction instead of one per record
+        constexpr bool BATCH = TMAX == 1 && CA * JPP == 16;
         for (int rc = hi - 1; rc >= lo; rc -= CA) {
+            float vb[BATCH ? CA * JPP : 1];
+#pragma unroll
+            for (int e = 0; e < (BATCH ? CA * JPP : 1); ++e) vb[e] = 0.f;
             float ac[CA][NPL];
 #pragma unroll
             for (int q = 0; q < CA; ++q) {
@@ -880,15 +887,20 @@ __device__ __forceinline__ bool kda_scan(const ReplayParams &p, uint8_t *cx, con
                         }
                     }
                 }
-                RowReduce<JPP, JPP, 1, 16, 0>::run(v, lane);
-                const int sh = 5 - LJ;
-                if ((lane & ((1 << sh) - 1)) == 0) {
-                    const int jj = lane >> sh;
-                    if (jj < TMAX) {
-                        if (jj < T) c1[(hd * TMAX + jj) * cap + r] = r < hc + jj ? v[0] : 0.f;
-                    } else if (jj < JP && jj - TMAX < T) {
-                        const int i = jj - TMAX;
-                        c2[(hd * TMAX + i) * cap + r] = r <= hc + i ? v[0] : 0.f;
+                if constexpr (BATCH) {
+#pragma unroll
+                    for (int jj = 0; jj < JPP; ++jj) vb[(BATCH ? q * JPP : 0) + jj] = v[jj];
+                } else {
+                    RowReduce<JPP, JPP, 1, 16, 0>::run(v, lane);
+                    const int sh = 5 - LJ;
+                    if ((lane & ((1 << sh) - 1)) == 0) {
+                        const int jj = lane >> sh;
+                        if (jj < TMAX) {
+                            if (jj < T) c1[(hd * TMAX + jj) * cap + r] = r < hc + jj ? v[0] : 0.f;
+                        } else if (jj < JP && jj - TMAX < T) {
+                            const int i = jj - TMAX;
+                            c2[(hd * TMAX + i) * cap + r] = r <= hc + i ? v[0] : 0.f;
+                        }
                     }
                 }
             }
@@ -904,6 +916,21 @@ __device__ __forceinline__ bool kda_scan(const ReplayParams &p, uint8_t *cx, con
                 if (r < F) PF[t] *= a[t];
             }
         }
+            if constexpr (BATCH) {
+                if (T > 0) {
+                    // lane 2e holds entry e = q JPP + jj: record rc - q, slot jj
+                    RowReduce<BATCH ? CA * JPP : 1, BATCH ? CA * JPP : 1, 1, 16, 0>::run(vb, lane);
+                    const int e = lane >> 1, q = e / JPP, jj = e % JPP, r = rc - q;
+                    if ((lane & 1) == 0 && r >= lo) {
+                        if (jj < TMAX) {
+                            if (jj < T) c1[(hd * TMAX + jj) * cap + r] = r < hc + jj ? vb[0] : 0.f;
+                        } else if (jj < JP && jj - TMAX < T) {
+                            const int i = jj - TMAX;
+                            c2[(hd * TMAX + i) * cap + r] = r <= hc + i ? vb[0] : 0.f;
+                        }
+                    }
+                }
+            }
         }
         // the warp whose chunk ends at record 0 now holds gamma(m_i) and gamma(F - 1)
         if (lo != 0 || (hi == 0 && ci != 0)) continue;
